@@ -148,8 +148,10 @@ static int quant_group(const uint16_t* w, const float* s, uint8_t* q,
     uint16_t sh = awqo_d2h_rn((double)d);
     if ((sh & 0x7C00) == 0x7C00) return OR_ERR_NONFINITE;
     double scale = awqo_h2d(sh);
+    /* the zero-point is an integer level 0..15; the clamp maps -0 (from
+     * rint of a negative quotient above -0.5) to the integer 0, i.e. +0.0 */
     float zf = rintf((float)(-(double)lo / scale));
-    if (zf < 0.0f) zf = 0.0f;
+    if (!(zf > 0.0f)) zf = 0.0f;
     if (zf > 15.0f) zf = 15.0f;
     for (int k = 0; k < GROUP; ++k) {
         float t = (float)((double)wp[k] / scale);

@@ -221,6 +221,10 @@ def test_quantizer_edge_groups(oracle_mod):
     z = ze.view(np.float16).astype(np.float64)[:, 0]
     assert np.all(scale >= 2.0 ** -14)
     assert scale[0] == 2.0 ** -14 and z[0] == 0 and np.all(q[0] == 0)   # zeros stay 0
+    # zero-points are the integers 0..15 in fp16, +0.0 for zero (never -0.0)
+    allowed = {oracle_mod.d2h_rn(float(v)) for v in range(16)}
+    assert 0x0000 in allowed and 0x8000 not in allowed
+    assert set(np.unique(ze).tolist()) <= allowed
     # one-signed groups: zero-point clamps, levels still ordered with w
     for r in (6, 7):
         assert np.all(np.diff(q[r].astype(int)) >= 0)
