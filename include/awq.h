@@ -1,0 +1,184 @@
+/*
+ * awq.h -- C ABI of the B300 (sm_103a) AWQ hot-path library libawq_b300.so.
+ *
+ * The method: "AWQ: Activation-aware Weight Quantization for On-Device LLM
+ * Compression and Acceleration" (fdeinterviews.com/papers/awq).  Third
+ * paragraph: multiplying a weight channel by s > 1 and dividing its input by
+ * s leaves a layer's output unchanged while shrinking that channel's relative
+ * rounding error; s is the channel's average activation magnitude raised to a
+ * power alpha, and alpha comes from a quick grid search on a small
+ * calibration set; every weight stays in low bits.  Sixth paragraph: only
+ * activation statistics are collected.  First paragraph: decoding reads
+ * every weight once per step and is memory-bound, so 4-bit weights cut its
+ * traffic about 4x.  The OpenAlex record of the same title (abstract):
+ * on-the-fly dequantisation and kernel fusion in the inference kernels.
+ * Group size 128, asymmetric levels 0..15 with fp16 scale and zero-point,
+ * mean |x| as the magnitude and output MSE as the search objective are this
+ * library's stated workload definition; the pages leave them open.
+ *
+ * Conventions for every call:
+ *  - Pointers are DEVICE pointers owned by the caller unless stated
+ *    otherwise.  The library never allocates device memory; scratch comes from
+ *    a caller-provided workspace of at least the size its *_workspace_size()
+ *    function returns (16-byte aligned).
+ *  - fp16 data is passed as uint16_t bit patterns (IEEE binary16), so this
+ *    header needs no CUDA header.  Matrices are row-major with the stated
+ *    leading dimension (elements).
+ *  - Calls are asynchronous and stream-ordered on `stream` (NULL = legacy
+ *    default stream).  Host-side argument errors are returned immediately and
+ *    nothing is launched.  Conditions found on the device (non-finite input,
+ *    a bounded wait that expired) are recorded in a library status word on
+ *    the current device; awq_sync_status() synchronises the stream and
+ *    returns and clears it.
+ *  - Calls that share a workspace race if they overlap on the GPU.
+ *  - Requires a compute capability 10.3 device (B300); others get
+ *    AWQ_ERR_DEVICE.
+ */
+#ifndef AWQ_B300_H
+#define AWQ_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int awq_status;
+enum {
+    AWQ_OK = 0,
+    AWQ_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad flag */
+    AWQ_ERR_SHAPE = 2,       /* K % 128 != 0, group != 128, N % 8 != 0, ld < K */
+    AWQ_ERR_ALIGN = 3,       /* pointer not 16-byte aligned or ld not a multiple of 8 */
+    AWQ_ERR_DEVICE = 4,      /* current device is not sm_103 / no kernel image */
+    AWQ_ERR_WORKSPACE = 5,   /* workspace missing or too small */
+    AWQ_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed */
+    AWQ_ERR_TIMEOUT = 7,     /* a bounded device-side wait expired */
+    AWQ_ERR_NONFINITE = 8    /* NaN/Inf input, or a group scale overflowing fp16 */
+};
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* awq_stream_t;
+
+#define AWQ_GROUP 128
+#define AWQ_MAX_ALPHAS 64
+
+/* ---- step: calibration statistics ---------------------------------------
+ * Per-input-channel sum of |x| over calibration tokens (the pages' "average
+ * activation magnitude", third paragraph; statistics only, sixth paragraph).
+ *   X            [T, K] fp16, leading dimension ldx (>= K, multiple of 8),
+ *                16-byte aligned; K % 8 == 0.
+ *   accumulate   0: abs_sum_q24 is overwritten; 1: this batch is added to
+ *                it (stream calibration batches through one buffer).
+ *   abs_sum_q24  [K] int64: sum_t |X[t,k]| * 2^24.  Every finite fp16 is an
+ *                integer multiple of 2^-24, so the sums are exact integers
+ *                and independent of summation order (bit-reproducible) for
+ *                fewer than 2^23 tokens in total.
+ * NaN/Inf inputs are skipped and flag AWQ_ERR_NONFINITE in the status word. */
+awq_status awq_act_stats(const uint16_t* X, int64_t T, int64_t K, int64_t ldx,
+                         int accumulate, int64_t* abs_sum_q24, awq_stream_t stream);
+
+/* mean_abs[k] = abs_sum_q24[k] / 2^24 / n_tokens (two IEEE fp64 divisions).
+ *   abs_sum_q24 [K] int64 (device), mean_abs [K] fp64 (device), n_tokens > 0. */
+awq_status awq_act_mean(const int64_t* abs_sum_q24, int64_t n_tokens, int64_t K,
+                        double* mean_abs, awq_stream_t stream);
+
+/* ---- step: candidate scales ---------------------------------------------
+ * s = mean|x|^alpha, normalised (third paragraph).  For each alpha_i:
+ *   r_k = pow(max(mean_abs[k], 1e-4), alpha_i)          (fp64)
+ *   s_alpha[i*K + k] = fp32( r_k / sqrt(max_j r_j * min_j r_j) )
+ * The normaliser only centres s around 1: a constant factor on s leaves the
+ * quantised layer's output unchanged.
+ *   mean_abs  [K] fp64 device.   alphas: HOST array of n_alpha fp64,
+ *   1 <= n_alpha <= AWQ_MAX_ALPHAS.   s_alpha [n_alpha, K] fp32 device.
+ *   workspace >= awq_candidate_scales_workspace_size(K, n_alpha) bytes. */
+awq_status awq_candidate_scales(const double* mean_abs, int64_t K, const double* alphas,
+                                int n_alpha, float* s_alpha, void* workspace,
+                                size_t ws_bytes, awq_stream_t stream);
+size_t awq_candidate_scales_workspace_size(int64_t K, int n_alpha);
+
+/* ---- step: alpha grid search ---------------------------------------------
+ * For every alpha on the grid (third paragraph: "quick grid search on a
+ * small calibration set", no backpropagation or reconstruction):
+ *   s = candidate scales (above); fake-quantise W diag(s) exactly as
+ *   awq_pack_int4 does; E = Q(W diag(s)) diag(s)^-1 - W;
+ *   mse(alpha) = ||Xcal E^T||_F^2 / (T N), the output MSE of
+ *   Q(W diag(s)) diag(s)^-1 Xcal against W Xcal.
+ * The best alpha is the smallest index with the least mse (ascending scan,
+ * strict <).  Xcal E^T runs on the tensor cores (fp16 E, fp32 accumulation).
+ *   W        [N, K] fp16, leading dimension ldw (>= K, multiple of 8).
+ *   Xcal     [T, K] fp16, leading dimension ldx (>= K, multiple of 8).
+ *   mean_abs [K] fp64 from awq_act_mean.
+ *   alphas   HOST array of n_alpha fp64, 1 <= n_alpha <= AWQ_MAX_ALPHAS.
+ *   group    must be 128.
+ *   s_out    [K] fp32: s at the best alpha.
+ *   mse_out  [n_alpha] fp64, may be NULL.
+ *   best_idx [1] int32.
+ *   s_alpha_out [n_alpha, K] fp32, may be NULL (all candidates, for checks).
+ * K % 128 == 0, N % 8 == 0, T >= 1.  Pointers 16-byte aligned.
+ * workspace >= awq_search_workspace_size(N, K, T, n_alpha) bytes. */
+awq_status awq_search_scale(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                            const uint16_t* Xcal, int64_t T, int64_t ldx,
+                            const double* mean_abs, const double* alphas, int n_alpha,
+                            int group, float* s_out, double* mse_out, int32_t* best_idx,
+                            float* s_alpha_out, void* workspace, size_t ws_bytes,
+                            awq_stream_t stream);
+size_t awq_search_workspace_size(int64_t N, int64_t K, int64_t T, int n_alpha);
+
+/* ---- step: INT4 packing --------------------------------------------------
+ * Low-bit weights (third paragraph: "every weight stays in low bits"; last
+ * paragraph: 4 bits).  Per row n and group g of 128 input channels:
+ *   w'_k  = fp32(W[n,k] * s_k)                     (s_k = 1 when s is NULL)
+ *   lo,hi = min, max of w' over the group
+ *   scale = fp16_rn(max(fp32(fp32(hi - lo) / 15), 2^-14))
+ *   z     = clamp(rint(fp32(-lo / scale)), 0, 15)
+ *   q_k   = clamp(rint(fp32(w'_k / scale)) + z, 0, 15)     (rint: ties to even)
+ * and dequantisation is (q - z) * scale.
+ *   W        [N, K] fp16, leading dimension ldw.
+ *   s        [K] fp32 (from awq_search_scale) or NULL for plain rounding.
+ *   group    must be 128.
+ *   qweight  [N, K/8] uint32: element k of row n in word k/8 of that row,
+ *            bits 4*(k%8) .. 4*(k%8)+3.
+ *   scales   [N, K/128] fp16.     zeros [N, K/128] fp16 holding 0..15.
+ * K % 128 == 0; pointers 16-byte aligned (scales/zeros: 2-byte). */
+awq_status awq_pack_int4(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                         const float* s, int group, uint32_t* qweight, uint16_t* scales,
+                         uint16_t* zeros, awq_stream_t stream);
+
+/* ---- step: dequantise-fused matmul -----------------------------------------
+ * Y = X deq(Wq)^T, deq = (q - z) * scale, fp32 accumulation, fp16 out
+ * (pages: fused 4-bit kernels; on-the-fly dequantisation; memory-bound
+ * decoding at small batch, more compute-bound at large batch).
+ *   X        [M, K] fp16, leading dimension ldx (>= K, multiple of 8); the
+ *            caller has already divided X by s (the pages' "divide its input
+ *            by s", normally folded into the previous operation).
+ *   qweight, scales, zeros: as written by awq_pack_int4 for an [N, K] weight.
+ *   Y        [M, N] fp16, leading dimension ldy (>= N).
+ * M <= 16 runs the decode kernel (packed weights streamed once, dequantised
+ * in registers); M > 16 runs the tcgen05 tensor-core kernel.
+ * workspace >= w4a16_gemm_workspace_size(M, N, K) bytes (may be 0/NULL when
+ * that size is 0).  K % 128 == 0, N % 8 == 0, group == 128. */
+awq_status w4a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
+                      const uint32_t* qweight, const uint16_t* scales, const uint16_t* zeros,
+                      int64_t N, int group, uint16_t* Y, int64_t ldy, void* workspace,
+                      size_t ws_bytes, awq_stream_t stream);
+size_t w4a16_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/* ---- status and diagnostics ---------------------------------------------- */
+
+/* Synchronise `stream`, then return (and clear) the device-side status word
+ * of the current device: AWQ_OK, AWQ_ERR_NONFINITE or AWQ_ERR_TIMEOUT
+ * (the most severe seen since the last call), or AWQ_ERR_CUDA if the
+ * synchronisation itself failed. */
+awq_status awq_sync_status(awq_stream_t stream);
+
+/* Static text for the last error returned by a call on this host thread. */
+const char* awq_last_error_string(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int awq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AWQ_B300_H */

@@ -1,0 +1,86 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every function
+declared in include/awq.h, and rejects bad arguments on the host before any
+device work (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "awq.h")
+
+
+@pytest.fixture(scope="module")
+def capi():
+    from weight_only_bit_stats_b300 import build
+    build.build()
+    import weight_only_bit_stats_b300 as wb
+    return wb.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for n in ("awq_act_stats", "awq_search_scale", "awq_pack_int4", "w4a16_gemm"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(capi):
+    import weight_only_bit_stats_b300 as wb
+    names = declared_functions()
+    bound = {n for n, _, _ in wb.SIGNATURES}
+    for n in names:
+        assert hasattr(capi, n), f"{n} not exported"
+        assert n in bound, f"{n} has no binding signature"
+
+
+def test_version_and_workspace_sizes(capi):
+    assert capi.awq_version() >= 100
+    assert capi.w4a16_gemm_workspace_size(1, 4096, 4096) == 0
+    n = capi.awq_search_workspace_size(12288, 4096, 512, 20)
+    # s_alpha + 1/s (fp32) + r (fp64) per alpha and channel, plus partials
+    assert n >= 20 * 4096 * (4 + 4 + 8) + 20 * 96 * 4 * 8
+    assert capi.awq_search_workspace_size(0, 4096, 512, 20) == 0
+    assert capi.awq_candidate_scales_workspace_size(4096, 20) >= 20 * 4096 * 8
+
+
+def test_host_argument_checks(capi):
+    """Bad arguments are refused before any device call."""
+    buf = ctypes.create_string_buffer(4096 + 16)
+    base = (ctypes.addressof(buf) + 15) & ~15
+    # null pointers
+    assert capi.awq_pack_int4(None, 8, 128, 128, None, 128, None, None, None, None) == 1
+    # group must be 128, K a multiple of 128
+    assert capi.awq_pack_int4(base, 8, 128, 128, None, 64, base, base, base, None) == 2
+    assert capi.awq_pack_int4(base, 8, 100, 100, None, 128, base, base, base, None) == 2
+    # misaligned weight pointer
+    assert capi.awq_pack_int4(base + 2, 8, 128, 128, None, 128, base, base, base, None) == 3
+    # gemm: N % 8, ldx < K
+    assert capi.w4a16_gemm(base, 1, 128, 128, base, base, base, 12, 128, base, 12, None, 0,
+                           None) == 2
+    assert capi.w4a16_gemm(base, 1, 256, 128, base, base, base, 16, 128, base, 16, None, 0,
+                           None) == 2
+    # search: too many alphas; missing workspace
+    alphas = (ctypes.c_double * 65)(*([0.0] * 65))
+    assert capi.awq_search_scale(base, 8, 128, 128, base, 4, 128, base, alphas, 65, 128, base,
+                                 None, base, None, base, 4096, None) == 1
+    assert capi.awq_search_scale(base, 8, 128, 128, base, 4, 128, base, alphas, 2, 128, base,
+                                 None, base, None, None, 0, None) == 5
+    # stats: bad accumulate flag
+    assert capi.awq_act_stats(base, 4, 128, 128, 2, base, None) == 1
+    assert capi.awq_last_error_string()
+
+
+def test_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    import weight_only_bit_stats_b300 as wb
+    with pytest.raises(ValueError):
+        wb.pack_int4(torch.zeros(8, 128, dtype=torch.float16))

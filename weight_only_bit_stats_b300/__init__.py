@@ -1,0 +1,218 @@
+"""Python binding of libawq_b300.so: the AWQ hot path on one B300 (sm_103a).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+Tensors must be CUDA tensors on the current device; results are produced on
+``torch.cuda.current_stream()``.  There is no CPU fallback: if the library is
+missing, importing the binding's functions raises.
+
+Steps (names follow the C ABI in ``include/awq.h``):
+
+* ``act_stats`` / ``act_mean``  -- per-input-channel mean |x| (exact sums)
+* ``candidate_scales``          -- s = mean|x|^alpha, normalised
+* ``search_scale``              -- alpha grid search by output MSE
+* ``pack_int4``                 -- asymmetric INT4, group 128, fp16 scale/zero
+* ``w4a16_gemm``                -- Y = X deq(Wq)^T, fp32 accumulate, fp16 out
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = ["AwqError", "lib", "act_stats", "act_mean", "candidate_scales", "search_scale",
+           "pack_int4", "w4a16_gemm", "sync_status", "ALPHA_GRID", "GROUP"]
+
+GROUP = 128
+ALPHA_GRID = tuple(i / 20.0 for i in range(20))
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libawq_b300.so")
+
+_STATUS = {0: "AWQ_OK", 1: "AWQ_ERR_INVALID_ARG", 2: "AWQ_ERR_SHAPE", 3: "AWQ_ERR_ALIGN",
+           4: "AWQ_ERR_DEVICE", 5: "AWQ_ERR_WORKSPACE", 6: "AWQ_ERR_CUDA", 7: "AWQ_ERR_TIMEOUT",
+           8: "AWQ_ERR_NONFINITE"}
+
+
+class AwqError(RuntimeError):
+    def __init__(self, code: int, where: str, msg: str):
+        super().__init__(f"{where}: {_STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_sz = ctypes.c_size_t
+
+# (name, restype, argtypes)
+SIGNATURES = (
+    ("awq_act_stats", _int, [_p, _i64, _i64, _i64, _int, _p, _p]),
+    ("awq_act_mean", _int, [_p, _i64, _i64, _p, _p]),
+    ("awq_candidate_scales", _int, [_p, _i64, _p, _int, _p, _p, _sz, _p]),
+    ("awq_candidate_scales_workspace_size", _sz, [_i64, _int]),
+    ("awq_search_scale", _int, [_p, _i64, _i64, _i64, _p, _i64, _i64, _p, _p, _int, _int, _p, _p,
+                                _p, _p, _p, _sz, _p]),
+    ("awq_search_workspace_size", _sz, [_i64, _i64, _i64, _int]),
+    ("awq_pack_int4", _int, [_p, _i64, _i64, _i64, _p, _int, _p, _p, _p, _p]),
+    ("w4a16_gemm", _int, [_p, _i64, _i64, _i64, _p, _p, _p, _i64, _int, _p, _i64, _p, _sz, _p]),
+    ("w4a16_gemm_workspace_size", _sz, [_i64, _i64, _i64]),
+    ("awq_sync_status", _int, [_p]),
+    ("awq_last_error_string", ctypes.c_char_p, []),
+    ("awq_version", _int, []),
+)
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -m weight_only_bit_stats_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, res, args in SIGNATURES:
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def _check(code: int, where: str) -> None:
+    if code != 0:
+        raise AwqError(code, where, lib().awq_last_error_string().decode())
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> torch.Tensor:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() >= 1 and t.stride(-1) != 1:
+        raise ValueError(f"{name} must have a contiguous last dimension")
+    return t
+
+
+def _ld(t: torch.Tensor) -> int:
+    return t.stride(0) if t.dim() == 2 else t.shape[-1]
+
+
+def act_stats(X: torch.Tensor, abs_sum: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Exact per-channel sum of |x| * 2^24 (int64 [K]).  With ``abs_sum``
+    given, this batch is added to it (streamed calibration)."""
+    _dev(X, torch.float16, "X")
+    T, K = X.shape
+    acc = abs_sum is not None
+    out = abs_sum if acc else torch.empty(K, dtype=torch.int64, device=X.device)
+    _dev(out, torch.int64, "abs_sum")
+    _check(lib().awq_act_stats(X.data_ptr(), T, K, _ld(X), int(acc), out.data_ptr(),
+                               _stream(stream)), "awq_act_stats")
+    return out
+
+
+def act_mean(abs_sum: torch.Tensor, n_tokens: int, stream=None) -> torch.Tensor:
+    """mean |x| per channel, fp64 [K]."""
+    _dev(abs_sum, torch.int64, "abs_sum")
+    out = torch.empty(abs_sum.shape[0], dtype=torch.float64, device=abs_sum.device)
+    _check(lib().awq_act_mean(abs_sum.data_ptr(), int(n_tokens), abs_sum.shape[0], out.data_ptr(),
+                              _stream(stream)), "awq_act_mean")
+    return out
+
+
+def _alphas(alphas) -> tuple[ctypes.Array, int]:
+    a = [float(x) for x in alphas]
+    return (ctypes.c_double * len(a))(*a), len(a)
+
+
+def candidate_scales(mean_abs: torch.Tensor, alphas=ALPHA_GRID, stream=None) -> torch.Tensor:
+    """All candidate scales, fp32 [n_alpha, K]."""
+    _dev(mean_abs, torch.float64, "mean_abs")
+    K = mean_abs.shape[0]
+    arr, n = _alphas(alphas)
+    out = torch.empty((n, K), dtype=torch.float32, device=mean_abs.device)
+    ws_n = lib().awq_candidate_scales_workspace_size(K, n)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=mean_abs.device)
+    _check(lib().awq_candidate_scales(mean_abs.data_ptr(), K, arr, n, out.data_ptr(),
+                                      ws.data_ptr(), ws_n, _stream(stream)), "awq_candidate_scales")
+    return out
+
+
+def search_workspace(N: int, K: int, T: int, n_alpha: int, device) -> torch.Tensor:
+    n = lib().awq_search_workspace_size(N, K, T, n_alpha)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def search_scale(W: torch.Tensor, Xcal: torch.Tensor, mean_abs: torch.Tensor, alphas=ALPHA_GRID,
+                 workspace: torch.Tensor | None = None, return_candidates: bool = False,
+                 stream=None):
+    """alpha grid search.  Returns ``(s fp32 [K], mse fp64 [n_alpha],
+    best int32 [1])`` (+ all candidate scales [n_alpha, K] when
+    ``return_candidates``), all on the device."""
+    _dev(W, torch.float16, "W")
+    _dev(Xcal, torch.float16, "Xcal")
+    _dev(mean_abs, torch.float64, "mean_abs")
+    N, K = W.shape
+    T = Xcal.shape[0]
+    arr, n = _alphas(alphas)
+    dev = W.device
+    s = torch.empty(K, dtype=torch.float32, device=dev)
+    mse = torch.empty(n, dtype=torch.float64, device=dev)
+    best = torch.empty(1, dtype=torch.int32, device=dev)
+    cands = torch.empty((n, K), dtype=torch.float32, device=dev) if return_candidates else None
+    if workspace is None:
+        workspace = search_workspace(N, K, T, n, dev)
+    _check(lib().awq_search_scale(W.data_ptr(), N, K, _ld(W), Xcal.data_ptr(), T, _ld(Xcal),
+                                  mean_abs.data_ptr(), arr, n, GROUP, s.data_ptr(), mse.data_ptr(),
+                                  best.data_ptr(), cands.data_ptr() if cands is not None else None,
+                                  workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "awq_search_scale")
+    return (s, mse, best, cands) if return_candidates else (s, mse, best)
+
+
+def pack_int4(W: torch.Tensor, s: torch.Tensor | None = None, out=None, stream=None):
+    """INT4 pack of W diag(s): ``(qweight int32 [N, K/8] (uint32 bits),
+    scales fp16 [N, K/128], zeros fp16 [N, K/128])``."""
+    _dev(W, torch.float16, "W")
+    N, K = W.shape
+    if s is not None:
+        _dev(s, torch.float32, "s")
+    if out is None:
+        out = (torch.empty((N, K // 8), dtype=torch.int32, device=W.device),
+               torch.empty((N, K // GROUP), dtype=torch.float16, device=W.device),
+               torch.empty((N, K // GROUP), dtype=torch.float16, device=W.device))
+    qw, sc, ze = out
+    _check(lib().awq_pack_int4(W.data_ptr(), N, K, _ld(W), s.data_ptr() if s is not None else None,
+                               GROUP, qw.data_ptr(), sc.data_ptr(), ze.data_ptr(), _stream(stream)),
+           "awq_pack_int4")
+    return qw, sc, ze
+
+
+def w4a16_gemm(X: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,
+               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y = X deq(Wq)^T, fp16 [M, N]."""
+    _dev(X, torch.float16, "X")
+    _dev(qweight, torch.int32, "qweight")
+    _dev(scales, torch.float16, "scales")
+    _dev(zeros, torch.float16, "zeros")
+    M, K = X.shape
+    N = qweight.shape[0]
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=X.device)
+    ws_n = lib().w4a16_gemm_workspace_size(M, N, K)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=X.device) if ws_n else None
+    _check(lib().w4a16_gemm(X.data_ptr(), M, K, _ld(X), qweight.data_ptr(), scales.data_ptr(),
+                            zeros.data_ptr(), N, GROUP, Y.data_ptr(), _ld(Y),
+                            ws.data_ptr() if ws is not None else None, ws_n, _stream(stream)),
+           "w4a16_gemm")
+    return Y
+
+
+def sync_status(stream=None) -> None:
+    """Synchronise and raise if a kernel flagged a device-side condition."""
+    _check(lib().awq_sync_status(_stream(stream)), "awq_sync_status")

@@ -1,0 +1,341 @@
+// C ABI of libawq_b300.so (declared in include/awq.h): argument checks,
+// workspace carving, TMA descriptor creation and kernel dispatch.  The
+// library allocates no device memory; every scratch buffer comes from the
+// caller's workspace.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "awq.h"
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace {
+
+// Device status word (one per device that loads the library).
+__device__ unsigned int g_awq_status;
+
+thread_local const char* g_last_error = "no error";
+
+constexpr int kMaxDevices = 64;
+struct DevInfo {
+    bool init = false;
+    bool ok = false;
+    int num_sms = 0;
+    unsigned* status = nullptr;
+};
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+awq_status fail(awq_status code, const char* msg) {
+    g_last_error = msg;
+    return code;
+}
+
+awq_status cuda_fail(cudaError_t e) {
+    g_last_error = cudaGetErrorString(e);
+    return AWQ_ERR_CUDA;
+}
+
+// Current device's info; checks compute capability 10.3 once per device.
+awq_status device_info(DevInfo** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return fail(AWQ_ERR_DEVICE, "device index out of range");
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DevInfo& d = g_dev[dev];
+    if (!d.init) {
+        d.init = true;
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_awq_status);
+        d.status = static_cast<unsigned*>(p);
+        d.ok = (major == 10 && minor == 3 && e == cudaSuccess && d.status != nullptr);
+        if (e != cudaSuccess) cudaGetLastError();
+    }
+    if (!d.ok) return fail(AWQ_ERR_DEVICE, "requires a compute capability 10.3 (sm_103a) device");
+    *out = &d;
+    return AWQ_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+awq_status make_act_map(CUtensorMap* map, const uint16_t* X, int64_t rows, int64_t K, int64_t ld) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return fail(AWQ_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)awq::kTcTokens};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(X), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(AWQ_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    return AWQ_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace layout of awq_search_scale / awq_candidate_scales.
+struct SearchWs {
+    size_t s_alpha, inv_s, r, mm, partials, mse, total;
+};
+SearchWs search_ws(int64_t N, int64_t K, int64_t T, int n_alpha) {
+    SearchWs w;
+    const int64_t n_tiles = (N + awq::kTcRows - 1) / awq::kTcRows;
+    const int64_t t_tiles = (T + awq::kSearchTokensPerItem - 1) / awq::kSearchTokensPerItem;
+    size_t off = 0;
+    w.s_alpha = off;  off += align256((size_t)n_alpha * K * 4);
+    w.inv_s = off;    off += align256((size_t)n_alpha * K * 4);
+    w.r = off;        off += align256((size_t)n_alpha * K * 8);
+    w.mm = off;       off += align256((size_t)n_alpha * awq::cand_blocks(K) * 2 * 8);
+    w.partials = off; off += align256((size_t)n_alpha * n_tiles * t_tiles * 4 * 8);
+    w.mse = off;      off += align256((size_t)n_alpha * 8);
+    w.total = off;
+    return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+int awq_version(void) { return 100; }
+
+const char* awq_last_error_string(void) { return g_last_error; }
+
+awq_status awq_sync_status(awq_stream_t stream) {
+    DevInfo* d = nullptr;
+    awq_status s = device_info(&d);
+    if (s) return s;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned v = 0;
+    e = cudaMemcpy(&v, d->status, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (v) {
+        unsigned zero = 0;
+        e = cudaMemcpy(d->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (v & awq::kStatusTimeout) return fail(AWQ_ERR_TIMEOUT, "a bounded device wait expired");
+    if (v & awq::kStatusNonFinite) return fail(AWQ_ERR_NONFINITE, "non-finite value on the device");
+    return AWQ_OK;
+}
+
+awq_status awq_act_stats(const uint16_t* X, int64_t T, int64_t K, int64_t ldx, int accumulate,
+                         int64_t* abs_sum_q24, awq_stream_t stream) {
+    if (T < 0 || K < 0 || (accumulate != 0 && accumulate != 1))
+        return fail(AWQ_ERR_INVALID_ARG, "act_stats: negative size or bad accumulate flag");
+    if (!abs_sum_q24 || (T > 0 && !X)) return fail(AWQ_ERR_INVALID_ARG, "act_stats: null pointer");
+    if (K % 8 || ldx < K || ldx % 8) return fail(AWQ_ERR_SHAPE, "act_stats: K and ldx must be multiples of 8, ldx >= K");
+    if ((X && !aligned16(X)) || (reinterpret_cast<uintptr_t>(abs_sum_q24) & 7u))
+        return fail(AWQ_ERR_ALIGN, "act_stats: X must be 16-byte aligned");
+    DevInfo* d = nullptr;
+    awq_status s = device_info(&d);
+    if (s) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaSuccess;
+    if (!accumulate && K > 0) e = cudaMemsetAsync(abs_sum_q24, 0, (size_t)K * 8, st);
+    if (e == cudaSuccess)
+        e = awq::launch_act_stats(X, T, K, ldx, reinterpret_cast<unsigned long long*>(abs_sum_q24),
+                                  d->status, d->num_sms, st);
+    return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
+}
+
+awq_status awq_act_mean(const int64_t* abs_sum_q24, int64_t n_tokens, int64_t K, double* mean_abs,
+                        awq_stream_t stream) {
+    if (n_tokens <= 0 || K < 0) return fail(AWQ_ERR_INVALID_ARG, "act_mean: n_tokens must be > 0");
+    if (K > 0 && (!abs_sum_q24 || !mean_abs)) return fail(AWQ_ERR_INVALID_ARG, "act_mean: null pointer");
+    DevInfo* d = nullptr;
+    awq_status s = device_info(&d);
+    if (s) return s;
+    cudaError_t e = awq::launch_act_mean(abs_sum_q24, n_tokens, K, mean_abs, (cudaStream_t)stream);
+    return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
+}
+
+size_t awq_candidate_scales_workspace_size(int64_t K, int n_alpha) {
+    if (K <= 0 || n_alpha <= 0) return 0;
+    return align256((size_t)n_alpha * K * 8) + align256((size_t)n_alpha * awq::cand_blocks(K) * 16);
+}
+
+awq_status awq_candidate_scales(const double* mean_abs, int64_t K, const double* alphas, int n_alpha,
+                                float* s_alpha, void* workspace, size_t ws_bytes,
+                                awq_stream_t stream) {
+    if (K <= 0 || n_alpha < 1 || n_alpha > AWQ_MAX_ALPHAS)
+        return fail(AWQ_ERR_INVALID_ARG, "candidate_scales: bad K or n_alpha");
+    if (!mean_abs || !alphas || !s_alpha) return fail(AWQ_ERR_INVALID_ARG, "candidate_scales: null pointer");
+    const size_t need = awq_candidate_scales_workspace_size(K, n_alpha);
+    if (!workspace || ws_bytes < need || !aligned16(workspace))
+        return fail(AWQ_ERR_WORKSPACE, "candidate_scales: workspace missing or too small");
+    DevInfo* d = nullptr;
+    awq_status s = device_info(&d);
+    if (s) return s;
+    awq::AlphaList al;
+    for (int i = 0; i < n_alpha; ++i) al.a[i] = alphas[i];
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    double* r = reinterpret_cast<double*>(ws);
+    double* mm = reinterpret_cast<double*>(ws + align256((size_t)n_alpha * K * 8));
+    cudaError_t e = awq::launch_candidate_scales(mean_abs, K, al, n_alpha, s_alpha, nullptr, r, mm,
+                                                 (cudaStream_t)stream);
+    return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
+}
+
+size_t awq_search_workspace_size(int64_t N, int64_t K, int64_t T, int n_alpha) {
+    if (N <= 0 || K <= 0 || T <= 0 || n_alpha <= 0) return 0;
+    return search_ws(N, K, T, n_alpha).total;
+}
+
+awq_status awq_search_scale(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                            const uint16_t* Xcal, int64_t T, int64_t ldx, const double* mean_abs,
+                            const double* alphas, int n_alpha, int group, float* s_out,
+                            double* mse_out, int32_t* best_idx, float* s_alpha_out,
+                            void* workspace, size_t ws_bytes, awq_stream_t stream) {
+    if (N <= 0 || K <= 0 || T <= 0 || n_alpha < 1 || n_alpha > AWQ_MAX_ALPHAS)
+        return fail(AWQ_ERR_INVALID_ARG, "search_scale: sizes must be positive, 1 <= n_alpha <= 64");
+    if (!W || !Xcal || !mean_abs || !alphas || !s_out || !best_idx)
+        return fail(AWQ_ERR_INVALID_ARG, "search_scale: null pointer");
+    if (group != AWQ_GROUP || K % AWQ_GROUP || N % 8 || ldw < K || ldx < K || ldw % 8 || ldx % 8)
+        return fail(AWQ_ERR_SHAPE, "search_scale: need group 128, K % 128 == 0, N % 8 == 0, ld >= K, ld % 8 == 0");
+    if (N > (1LL << 30) || T > (1LL << 30) || K > (1LL << 30))
+        return fail(AWQ_ERR_SHAPE, "search_scale: size too large");
+    if (!aligned16(W) || !aligned16(Xcal) || !aligned16(s_out) ||
+        (s_alpha_out && !aligned16(s_alpha_out)))
+        return fail(AWQ_ERR_ALIGN, "search_scale: W, Xcal, s_out must be 16-byte aligned");
+    const SearchWs lay = search_ws(N, K, T, n_alpha);
+    if (!workspace || ws_bytes < lay.total || !aligned16(workspace))
+        return fail(AWQ_ERR_WORKSPACE, "search_scale: workspace missing or too small");
+    DevInfo* d = nullptr;
+    awq_status s = device_info(&d);
+    if (s) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* s_alpha = s_alpha_out ? s_alpha_out : reinterpret_cast<float*>(ws + lay.s_alpha);
+    float* inv_s = reinterpret_cast<float*>(ws + lay.inv_s);
+    double* partials = reinterpret_cast<double*>(ws + lay.partials);
+    double* mse = mse_out ? mse_out : reinterpret_cast<double*>(ws + lay.mse);
+
+    awq::AlphaList al;
+    for (int i = 0; i < n_alpha; ++i) al.a[i] = alphas[i];
+    cudaError_t e = awq::launch_candidate_scales(mean_abs, K, al, n_alpha, s_alpha, inv_s,
+                                                 reinterpret_cast<double*>(ws + lay.r),
+                                                 reinterpret_cast<double*>(ws + lay.mm), st);
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    CUtensorMap map;
+    s = make_act_map(&map, Xcal, T, K, ldx);
+    if (s) return s;
+    awq::TcParams p = {};
+    p.N = (int)N;
+    p.K = (int)K;
+    p.G = (int)(K / AWQ_GROUP);
+    p.rows_tok = (int)T;
+    p.n_tiles = (int)((N + awq::kTcRows - 1) / awq::kTcRows);
+    p.t_tiles = (int)((T + awq::kSearchTokensPerItem - 1) / awq::kSearchTokensPerItem);
+    p.n_alpha = n_alpha;
+    p.n_items = p.n_tiles * p.t_tiles * n_alpha;
+    p.W = W;
+    p.ldw = ldw;
+    p.s_alpha = s_alpha;
+    p.inv_s_alpha = inv_s;
+    p.partials = partials;
+    p.status = d->status;
+    e = awq::launch_tc_search(map, p, d->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = awq::launch_search_finalize(partials, n_alpha, (int64_t)p.n_tiles * p.t_tiles * 4, T, N, K,
+                                    s_alpha, mse, best_idx, s_out, st);
+    return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
+}
+
+awq_status awq_pack_int4(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, const float* s,
+                         int group, uint32_t* qweight, uint16_t* scales, uint16_t* zeros,
+                         awq_stream_t stream) {
+    if (N < 0 || K < 0) return fail(AWQ_ERR_INVALID_ARG, "pack_int4: negative size");
+    if ((N > 0 && K > 0) && (!W || !qweight || !scales || !zeros))
+        return fail(AWQ_ERR_INVALID_ARG, "pack_int4: null pointer");
+    if (group != AWQ_GROUP || K % AWQ_GROUP || ldw < K || ldw % 8)
+        return fail(AWQ_ERR_SHAPE, "pack_int4: need group 128, K % 128 == 0, ldw >= K, ldw % 8 == 0");
+    if ((W && !aligned16(W)) || (qweight && !aligned16(qweight)) || (s && !aligned16(s)) ||
+        (reinterpret_cast<uintptr_t>(scales) & 1u) || (reinterpret_cast<uintptr_t>(zeros) & 1u))
+        return fail(AWQ_ERR_ALIGN, "pack_int4: W, qweight, s must be 16-byte aligned");
+    DevInfo* d = nullptr;
+    awq_status st_ = device_info(&d);
+    if (st_) return st_;
+    cudaError_t e = awq::launch_pack_int4(W, N, K, ldw, s, qweight, scales, zeros, d->status,
+                                          d->num_sms, (cudaStream_t)stream);
+    return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
+}
+
+size_t w4a16_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
+    (void)M;
+    (void)N;
+    (void)K;
+    return 0;
+}
+
+awq_status w4a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx, const uint32_t* qweight,
+                      const uint16_t* scales, const uint16_t* zeros, int64_t N, int group,
+                      uint16_t* Y, int64_t ldy, void* workspace, size_t ws_bytes,
+                      awq_stream_t stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    if (M < 0 || N < 0 || K < 0) return fail(AWQ_ERR_INVALID_ARG, "w4a16_gemm: negative size");
+    if (M == 0 || N == 0) return AWQ_OK;
+    if (!X || !qweight || !scales || !zeros || !Y)
+        return fail(AWQ_ERR_INVALID_ARG, "w4a16_gemm: null pointer");
+    if (group != AWQ_GROUP || K <= 0 || K % AWQ_GROUP || N % 8 || ldx < K || ldx % 8 || ldy < N)
+        return fail(AWQ_ERR_SHAPE, "w4a16_gemm: need group 128, K % 128 == 0, N % 8 == 0, ldx >= K, ldx % 8 == 0, ldy >= N");
+    if (M > (1LL << 30) || N > (1LL << 30) || K > (1LL << 30))
+        return fail(AWQ_ERR_SHAPE, "w4a16_gemm: size too large");
+    if (!aligned16(X) || !aligned16(qweight) || (reinterpret_cast<uintptr_t>(Y) & 1u) ||
+        (reinterpret_cast<uintptr_t>(scales) & 1u) || (reinterpret_cast<uintptr_t>(zeros) & 1u))
+        return fail(AWQ_ERR_ALIGN, "w4a16_gemm: X and qweight must be 16-byte aligned");
+    DevInfo* d = nullptr;
+    awq_status s = device_info(&d);
+    if (s) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e;
+    if (M <= 16) {
+        // the staged activations of one CTA must fit in shared memory
+        if (M * ((K / AWQ_GROUP + 7) / 8 * 256 + 64) + 64 * M * 4 > 200 * 1024)
+            return fail(AWQ_ERR_SHAPE, "w4a16_gemm: K too large for the decode kernel");
+        awq::GemvParams p = {X, ldx, (int)M, qweight, scales, zeros, N, K, (int)(K / AWQ_GROUP), Y, ldy};
+        e = awq::launch_gemv(p, d->num_sms, st);
+    } else {
+        CUtensorMap map;
+        s = make_act_map(&map, X, M, K, ldx);
+        if (s) return s;
+        awq::TcParams p = {};
+        p.N = (int)N;
+        p.K = (int)K;
+        p.G = (int)(K / AWQ_GROUP);
+        p.rows_tok = (int)M;
+        p.n_tiles = (int)((N + awq::kTcRows - 1) / awq::kTcRows);
+        p.t_tiles = (int)((M + awq::kGemmTokensPerItem - 1) / awq::kGemmTokensPerItem);
+        p.n_items = p.n_tiles * p.t_tiles;
+        p.qw = qweight;
+        p.scales = scales;
+        p.zeros = zeros;
+        p.Y = Y;
+        p.ldy = ldy;
+        p.status = d->status;
+        e = awq::launch_tc_gemm(map, p, d->num_sms, st);
+    }
+    return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// Host-side launchers of the library's kernels (private to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace awq {
+
+struct AlphaList {
+    double a[64];
+};
+
+// ---- statistics (stats.cu) ----
+cudaError_t launch_act_stats(const uint16_t* X, int64_t T, int64_t K, int64_t ldx,
+                             unsigned long long* abs_sum, unsigned* status, int num_sms,
+                             cudaStream_t st);
+cudaError_t launch_act_mean(const int64_t* abs_sum, int64_t n_tokens, int64_t K, double* mean,
+                            cudaStream_t st);
+
+// ---- candidate scales, pack, search reduction (quant.cu) ----
+int cand_blocks(int64_t K);
+// ws_r: [n_alpha, K] fp64; ws_mm: [n_alpha, cand_blocks(K), 2] fp64.
+cudaError_t launch_candidate_scales(const double* mean, int64_t K, const AlphaList& alphas,
+                                    int n_alpha, float* s_alpha, float* inv_s_alpha, double* ws_r,
+                                    double* ws_mm, cudaStream_t st);
+cudaError_t launch_pack_int4(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, const float* s,
+                             uint32_t* qweight, uint16_t* scales, uint16_t* zeros, unsigned* status,
+                             int num_sms, cudaStream_t st);
+// mse[a] = sum_i partials[a][i] / (T N) for i < n_part; best = first argmin;
+// s_out = s_alpha[best].
+cudaError_t launch_search_finalize(const double* partials, int n_alpha, int64_t n_part, int64_t T,
+                                   int64_t N, int64_t K, const float* s_alpha, double* mse,
+                                   int32_t* best_idx, float* s_out, cudaStream_t st);
+
+// ---- decode matmul, M <= 16 (gemv.cu) ----
+struct GemvParams {
+    const uint16_t* X;
+    int64_t ldx;
+    int M;
+    const uint32_t* qw;
+    const uint16_t* scales;
+    const uint16_t* zeros;
+    int64_t N, K;
+    int G;
+    uint16_t* Y;
+    int64_t ldy;
+};
+cudaError_t launch_gemv(const GemvParams& p, int num_sms, cudaStream_t st);
+
+// ---- tensor-core kernels (tc.cu): W4A16 GEMM and the alpha search ----
+struct TcParams {
+    int N, K, G;
+    int rows_tok;    // M (GEMM) or T (search): rows of the TMA-loaded activations
+    int n_tiles;     // ceil(N / 128)
+    int t_tiles;     // ceil(rows_tok / tokens per item)
+    int n_items;
+    // GEMM
+    const uint32_t* qw;
+    const uint16_t* scales;
+    const uint16_t* zeros;
+    uint16_t* Y;
+    int64_t ldy;
+    // search
+    const uint16_t* W;
+    int64_t ldw;
+    const float* s_alpha;
+    const float* inv_s_alpha;
+    int n_alpha;
+    double* partials;  // [n_alpha][n_tiles][t_tiles][4]
+    unsigned* status;
+};
+constexpr int kTcRows = 128;          // weight rows per tile (UMMA M)
+constexpr int kTcTokens = 256;        // tokens per accumulator slot (UMMA N)
+constexpr int kGemmTokensPerItem = 256;
+constexpr int kSearchTokensPerItem = 512;
+
+cudaError_t launch_tc_gemm(const CUtensorMap& mapX, const TcParams& p, int num_sms,
+                           cudaStream_t st);
+cudaError_t launch_tc_search(const CUtensorMap& mapX, const TcParams& p, int num_sms,
+                             cudaStream_t st);
+
+}  // namespace awq

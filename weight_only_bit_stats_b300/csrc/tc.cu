@@ -1,0 +1,474 @@
+// Tensor-core kernels on sm_103a (tcgen05 MMA, TMEM accumulators, TMA):
+//
+//  * W4A16 GEMM for M > 16 tokens: Y = X deq(Wq)^T.  Under large batches the
+//    matmul becomes compute-bound ("AWQ: Activation-aware Weight Quantization
+//    ...", fdeinterviews.com/papers/awq, "Weight-only quantization helps
+//    decoding most" paragraph); the packed tile is dequantised on the fly
+//    into shared memory and multiplied on the tensor cores (the OpenAlex
+//    record's abstract: on-the-fly dequantisation, kernel fusion).
+//  * The alpha search (third paragraph: grid search over alpha on a small
+//    calibration set): per alpha, the producer fake-quantises W diag(s) with
+//    the exact rounding of the packer and writes the residual
+//    E = Q(W diag(s)) diag(s)^-1 - W as fp16; the tensor cores form Xcal E^T
+//    and the epilogue reduces its squares -- the per-alpha output MSE is a
+//    fused epilogue and E never reaches global memory.
+//
+// One persistent CTA per SM.  Warp roles:
+//   warp 0      TMA producer of activation tiles (one thread)
+//   warp 1      MMA issuer (one thread): tcgen05.mma M=128 N=256 K=16
+//   warp 2      TMEM allocator (512 columns = two 256-column accumulators)
+//   warps 4..7  epilogue: tcgen05.ld of their TMEM lane quarter
+//   warps 8..   weight-operand producers (dequant or fake-quant)
+// Work item = 128 weight rows x (256 tokens for the GEMM, 512 for the
+// search, i.e. both accumulators), looping over K in groups of 128.
+// Operand tiles are K-major in the 128-byte swizzled layout; the A tile of
+// a group is two [128 x 64] sub-tiles, the B tile two [256 x 64] sub-tiles.
+// Every mbarrier wait is bounded; a timeout sets an abort flag that every
+// role checks, records AWQ's timeout status, and the CTA exits cleanly after
+// its own TMA copies and MMAs have drained and TMEM is freed.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace awq {
+namespace {
+
+enum { kModeGemm = 0, kModeSearch = 1 };
+
+constexpr int kNA = 2;                            // A (weight) stages
+constexpr int kNB = 2;                            // B (activation) stages
+constexpr int kAStage = kTcRows * kGroup * 2;     // 32 KB
+constexpr int kASub = kTcRows * 64 * 2;           // 16 KB
+constexpr int kBStage = kTcTokens * kGroup * 2;   // 64 KB
+constexpr int kBSub = kTcTokens * 64 * 2;         // 32 KB
+constexpr int kTmemCols = 512;
+
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpTmem = 2, kWarpEpi0 = 4, kWarpProd0 = 8;
+
+template <int MODE>
+struct Cfg {
+    static constexpr int kProdWarps = MODE == kModeGemm ? 4 : 16;
+    static constexpr int kThreads = (kWarpProd0 + kProdWarps) * 32;
+    static constexpr int kHalves = MODE == kModeGemm ? 1 : 2;   // accumulators per item
+};
+
+struct SmemCtl {
+    uint64_t a_full[kNA], a_empty[kNA];
+    uint64_t b_full[kNB], b_empty[kNB];
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t kSmemBytes = 1024 /*align slack*/ + kNA * kAStage + kNB * kBStage + sizeof(SmemCtl);
+
+struct Item {
+    int n_tile, t_tile, alpha;
+};
+
+template <int MODE>
+__device__ __forceinline__ Item decode_item(int item, const TcParams& p) {
+    Item it;
+    if (MODE == kModeGemm) {           // consecutive CTAs share the activation tile
+        it.n_tile = item % p.n_tiles;
+        it.t_tile = item / p.n_tiles;
+        it.alpha = 0;
+    } else {                           // consecutive CTAs share the weight tile
+        it.alpha = item % p.n_alpha;
+        const int rest = item / p.n_alpha;
+        it.t_tile = rest % p.t_tiles;
+        it.n_tile = rest / p.t_tiles;
+    }
+    return it;
+}
+
+// Bounded wait that ignores the abort flag (used only to drain own copies).
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+    unsigned long long t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > 100000000ull) break;
+    }
+}
+
+// ---- role: TMA producer of activation tiles ----
+template <int MODE>
+__device__ void role_tma(const CUtensorMap* mapX, const TcParams& p, uint8_t* Bs, SmemCtl* ctl) {
+    constexpr int H = Cfg<MODE>::kHalves;
+    volatile int* abort = &ctl->abort;
+    uint32_t b_iter = 0;
+    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+        const Item it = decode_item<MODE>(item, p);
+        const int t0 = it.t_tile * kTcTokens * H;
+        for (int g = 0; g < p.G; ++g) {
+            for (int h = 0; h < H; ++h) {
+                const int st = b_iter % kNB;
+                const uint32_t ph = (b_iter / kNB) & 1u;
+                if (!mbar_wait(&ctl->b_empty[st], ph ^ 1u, abort, p.status)) goto drain;
+                mbar_arrive_expect_tx(&ctl->b_full[st], kBStage);
+                uint8_t* dst = Bs + st * kBStage;
+                tma_load_2d(dst, mapX, &ctl->b_full[st], g * kGroup, t0 + h * kTcTokens);
+                tma_load_2d(dst + kBSub, mapX, &ctl->b_full[st], g * kGroup + 64,
+                            t0 + h * kTcTokens);
+                ++b_iter;
+            }
+        }
+    }
+    return;
+drain:
+    // wait (bounded) for the copies this thread issued into each stage
+    for (int d = 1; d <= kNB && (int)b_iter - d >= 0; ++d) {
+        const uint32_t i = b_iter - d;
+        mbar_drain(&ctl->b_full[i % kNB], (i / kNB) & 1u);
+    }
+}
+
+// ---- role: MMA issuer ----
+template <int MODE>
+__device__ void role_mma(const TcParams& p, uint8_t* As, uint8_t* Bs, SmemCtl* ctl, uint32_t tmem) {
+    constexpr int H = Cfg<MODE>::kHalves;
+    constexpr uint32_t idesc = umma_idesc_f16_f32(kTcRows, kTcTokens);
+    volatile int* abort = &ctl->abort;
+    uint32_t a_iter = 0, b_iter = 0, acc_iter = 0;
+    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+        for (int g = 0; g < p.G; ++g) {
+            const int sa = a_iter % kNA;
+            if (!mbar_wait(&ctl->a_full[sa], (a_iter / kNA) & 1u, abort, p.status)) goto out;
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(As + sa * kAStage);
+            for (int h = 0; h < H; ++h) {
+                const uint32_t slot_iter = acc_iter + h;
+                const int slot = slot_iter & 1;
+                if (g == 0) {
+                    if (!mbar_wait(&ctl->acc_empty[slot], ((slot_iter >> 1) & 1u) ^ 1u, abort,
+                                   p.status))
+                        goto out;
+                    tc_fence_after();
+                }
+                const int sb = b_iter % kNB;
+                if (!mbar_wait(&ctl->b_full[sb], (b_iter / kNB) & 1u, abort, p.status)) goto out;
+                tc_fence_after();
+                const uint32_t b_base = smem_u32(Bs + sb * kBStage);
+                const uint32_t d = tmem + (uint32_t)(slot * kTcTokens);
+#pragma unroll
+                for (int ks = 0; ks < kGroup / 16; ++ks) {
+                    const uint32_t sub = ks >> 2, koff = (ks & 3) * 32;
+                    const uint64_t ad = umma_desc_sw128(a_base + sub * kASub + koff);
+                    const uint64_t bd = umma_desc_sw128(b_base + sub * kBSub + koff);
+                    umma_f16(d, ad, bd, idesc, (g > 0 || ks > 0) ? 1u : 0u);
+                }
+                umma_commit(&ctl->b_empty[sb]);
+                ++b_iter;
+            }
+            umma_commit(&ctl->a_empty[sa]);
+            ++a_iter;
+        }
+        for (int h = 0; h < H; ++h) umma_commit(&ctl->acc_full[(acc_iter + h) & 1]);
+        acc_iter += H;
+    }
+out:
+    // every MMA this thread issued has finished before TMEM is released
+    umma_commit(&ctl->mma_done);
+    mbar_drain(&ctl->mma_done, 0);
+}
+
+// ---- role: epilogue ----
+template <int MODE>
+__device__ void role_epilogue(const TcParams& p, SmemCtl* ctl, uint32_t tmem, int q, int lane) {
+    constexpr int H = Cfg<MODE>::kHalves;
+    volatile int* abort = &ctl->abort;
+    uint32_t acc_iter = 0;
+    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+        const Item it = decode_item<MODE>(item, p);
+        const int64_t n = (int64_t)it.n_tile * kTcRows + q * 32 + lane;   // this thread's row
+        float sq = 0.0f;
+        for (int h = 0; h < H; ++h) {
+            const int slot = acc_iter & 1;
+            if (!mbar_wait(&ctl->acc_full[slot], (acc_iter >> 1) & 1u, abort, p.status)) return;
+            tc_fence_after();
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * kTcTokens);
+            const int64_t tok0 = ((int64_t)it.t_tile * H + h) * kTcTokens;
+#pragma unroll 1
+            for (int c = 0; c < kTcTokens / 32; ++c) {
+                float v[32];
+                tmem_ld32(taddr + c * 32, v);
+                if (MODE == kModeGemm) {
+                    if (n < p.N) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int64_t tok = tok0 + c * 32 + j;
+                            if (tok < p.rows_tok)
+                                p.Y[tok * p.ldy + n] = __half_as_ushort(__float2half_rn(v[j]));
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) sq = fmaf(v[j], v[j], sq);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->acc_empty[slot]);
+            ++acc_iter;
+        }
+        if (MODE == kModeSearch) {
+            // one fp64 partial per epilogue warp; the final reduction adds
+            // them in a fixed order
+            double d = (double)sq;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+            if (lane == 0)
+                p.partials[(((int64_t)it.alpha * p.n_tiles + it.n_tile) * p.t_tiles + it.t_tile) * 4 +
+                           q] = d;
+        }
+    }
+}
+
+// ---- role: GEMM weight producer (int4 -> exact fp16 (q - z) * scale) ----
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// 8 nibbles -> 8 consecutive fp16 (q - z) * scale, exact (|q - z| <= 15 and
+// an 11-bit scale significand give at most 15 significant bits).
+__device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 z1024, __half2 zneg64, __half2 sc) {
+    const uint32_t magic = 0x64006400u;
+    const __half2 sixteenth = __half2half2(__float2half_rn(0.0625f));
+    const uint32_t w8 = w >> 8;
+    __half2 p0 = __hsub2(u2h(lop3_and_or(w, 0x000F000Fu, magic)), z1024);           // e0 | e4
+    __half2 p1 = __hfma2(u2h(lop3_and_or(w, 0x00F000F0u, magic)), sixteenth, zneg64);  // e1 | e5
+    __half2 p2 = __hsub2(u2h(lop3_and_or(w8, 0x000F000Fu, magic)), z1024);          // e2 | e6
+    __half2 p3 = __hfma2(u2h(lop3_and_or(w8, 0x00F000F0u, magic)), sixteenth, zneg64); // e3 | e7
+    const uint32_t u0 = h2u(__hmul2(p0, sc)), u1 = h2u(__hmul2(p1, sc));
+    const uint32_t u2 = h2u(__hmul2(p2, sc)), u3 = h2u(__hmul2(p3, sc));
+    return make_uint4(prmt(u0, u1, 0x5410), prmt(u2, u3, 0x5410), prmt(u0, u1, 0x7632),
+                      prmt(u2, u3, 0x7632));
+}
+
+__device__ void role_prod_gemm(const TcParams& p, uint8_t* As, SmemCtl* ctl, int r, int lane) {
+    volatile int* abort = &ctl->abort;
+    const int64_t wstride = p.K / 8;
+    uint32_t a_iter = 0;
+    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+        const Item it = decode_item<kModeGemm>(item, p);
+        const int64_t n = (int64_t)it.n_tile * kTcRows + r;
+        const bool valid = n < p.N;
+        const uint4* qrow = reinterpret_cast<const uint4*>(p.qw + (valid ? n : 0) * wstride);
+        const uint16_t* srow = p.scales + (valid ? n : 0) * p.G;
+        const uint16_t* zrow = p.zeros + (valid ? n : 0) * p.G;
+        uint4 cur[4];
+        uint16_t csc = 0, cze = 0;
+        if (valid) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) cur[j] = __ldg(qrow + j);
+            csc = __ldg(srow);
+            cze = __ldg(zrow);
+        }
+        for (int g = 0; g < p.G; ++g) {
+            uint4 nxt[4];
+            uint16_t nsc = 0, nze = 0;
+            if (valid && g + 1 < p.G) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) nxt[j] = __ldg(qrow + (int64_t)(g + 1) * 4 + j);
+                nsc = __ldg(srow + g + 1);
+                nze = __ldg(zrow + g + 1);
+            }
+            const int st = a_iter % kNA;
+            if (!mbar_wait(&ctl->a_empty[st], ((a_iter / kNA) & 1u) ^ 1u, abort, p.status)) return;
+            uint8_t* tile = As + st * kAStage;
+            if (valid) {
+                const __half z = __ushort_as_half(cze);
+                const __half2 z1024 = __half2half2(__hadd(__float2half_rn(1024.0f), z));
+                const __half2 zneg = __half2half2(__hneg(__hadd(__float2half_rn(64.0f), z)));
+                const __half2 sc = __half2half2(__ushort_as_half(csc));
+                const uint32_t w[16] = {cur[0].x, cur[0].y, cur[0].z, cur[0].w, cur[1].x, cur[1].y,
+                                        cur[1].z, cur[1].w, cur[2].x, cur[2].y, cur[2].z, cur[2].w,
+                                        cur[3].x, cur[3].y, cur[3].z, cur[3].w};
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint4 o = dequant8(w[j], z1024, zneg, sc);
+                    const int k = j * 8;   // 0..120 within the group
+                    *reinterpret_cast<uint4*>(tile + (k >> 6) * kASub + sw128_offset(r, k & 63)) = o;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int k = j * 8;
+                    *reinterpret_cast<uint4*>(tile + (k >> 6) * kASub + sw128_offset(r, k & 63)) =
+                        make_uint4(0, 0, 0, 0);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->a_full[st]);
+            ++a_iter;
+            if (valid && g + 1 < p.G) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) cur[j] = nxt[j];
+                csc = nsc;
+                cze = nze;
+            }
+        }
+    }
+}
+
+// ---- role: search producer (fake-quantise W diag(s), residual E in fp16) ----
+// Warp pw handles rows pw, pw + 16, ..., of the 128-row tile; each lane holds
+// 4 consecutive channels of the group.  The quantiser is the packer's, with
+// the same single-rounding fp32 steps.
+template <int PW>
+__device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, int pw, int lane) {
+    constexpr int kRowsPerWarp = kTcRows / PW;
+    volatile int* abort = &ctl->abort;
+    uint32_t a_iter = 0;
+    bool bad = false;
+    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+        const Item it = decode_item<kModeSearch>(item, p);
+        const float* s_a = p.s_alpha + (int64_t)it.alpha * p.K;
+        const float* is_a = p.inv_s_alpha + (int64_t)it.alpha * p.K;
+        for (int g = 0; g < p.G; ++g) {
+            const int64_t k0 = (int64_t)g * kGroup + 4 * lane;
+            const float4 sv = __ldg(reinterpret_cast<const float4*>(s_a + k0));
+            const float4 iv = __ldg(reinterpret_cast<const float4*>(is_a + k0));
+            uint2 raw[kRowsPerWarp];
+#pragma unroll
+            for (int i = 0; i < kRowsPerWarp; ++i) {
+                const int64_t n = (int64_t)it.n_tile * kTcRows + pw + PW * i;
+                raw[i] = n < p.N ? __ldg(reinterpret_cast<const uint2*>(p.W + n * p.ldw + k0))
+                                 : make_uint2(0, 0);
+            }
+            const int st = a_iter % kNA;
+            if (!mbar_wait(&ctl->a_empty[st], ((a_iter / kNA) & 1u) ^ 1u, abort, p.status)) return;
+            uint8_t* tile = As + st * kAStage;
+#pragma unroll
+            for (int i = 0; i < kRowsPerWarp; ++i) {
+                const int r = pw + PW * i;
+                float w[4];
+                w[0] = __half2float(__ushort_as_half((unsigned short)(raw[i].x & 0xFFFFu)));
+                w[1] = __half2float(__ushort_as_half((unsigned short)(raw[i].x >> 16)));
+                w[2] = __half2float(__ushort_as_half((unsigned short)(raw[i].y & 0xFFFFu)));
+                w[3] = __half2float(__ushort_as_half((unsigned short)(raw[i].y >> 16)));
+                float wp[4];
+                wp[0] = __fmul_rn(w[0], sv.x);
+                wp[1] = __fmul_rn(w[1], sv.y);
+                wp[2] = __fmul_rn(w[2], sv.z);
+                wp[3] = __fmul_rn(w[3], sv.w);
+                float lo = fminf(fminf(wp[0], wp[1]), fminf(wp[2], wp[3]));
+                float hi = fmaxf(fmaxf(wp[0], wp[1]), fmaxf(wp[2], wp[3]));
+                bad |= !(isfinite(wp[0]) && isfinite(wp[1]) && isfinite(wp[2]) && isfinite(wp[3]));
+                const GroupQuant gq = group_quant_params(lo, hi);
+                bad |= !gq.finite;
+                const float is[4] = {iv.x, iv.y, iv.z, iv.w};
+                __half e[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float qf = quant_level(wp[j], gq);
+                    const float deq = __fmul_rn(__fsub_rn(qf, gq.zf), gq.scale);
+                    e[j] = __float2half_rn(__fmaf_rn(deq, is[j], -w[j]));
+                }
+                uint2 o;
+                o.x = (uint32_t)__half_as_ushort(e[0]) | ((uint32_t)__half_as_ushort(e[1]) << 16);
+                o.y = (uint32_t)__half_as_ushort(e[2]) | ((uint32_t)__half_as_ushort(e[3]) << 16);
+                const int k = 4 * lane;
+                *reinterpret_cast<uint2*>(tile + (k >> 6) * kASub + sw128_offset(r, k & 63)) = o;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->a_full[st]);
+            ++a_iter;
+        }
+    }
+    if (bad) set_status(p.status, kStatusNonFinite);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
+    tc_kernel(const __grid_constant__ CUtensorMap mapX, const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* As = smem;
+    uint8_t* Bs = smem + kNA * kAStage;
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(Bs + kNB * kBStage);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNA; ++i) {
+            mbar_init(&ctl->a_full[i], Cfg<MODE>::kProdWarps);
+            mbar_init(&ctl->a_empty[i], 1);
+        }
+        for (int i = 0; i < kNB; ++i) {
+            mbar_init(&ctl->b_full[i], 1);
+            mbar_init(&ctl->b_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctl->acc_full[i], 1);
+            mbar_init(&ctl->acc_empty[i], 4);
+        }
+        mbar_init(&ctl->mma_done, 1);
+        ctl->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kWarpTmem) {
+        tmem_alloc(&ctl->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kWarpTma && lane == 0) tma_prefetch_desc(&mapX);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+
+    if (warp == kWarpTma) {
+        if (lane == 0) role_tma<MODE>(&mapX, p, Bs, ctl);
+    } else if (warp == kWarpMma) {
+        if (lane == 0) role_mma<MODE>(p, As, Bs, ctl, tmem);
+    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
+        role_epilogue<MODE>(p, ctl, tmem, warp - kWarpEpi0, lane);
+    } else if (warp >= kWarpProd0) {
+        if (MODE == kModeGemm)
+            role_prod_gemm(p, As, ctl, (warp - kWarpProd0) * 32 + lane, lane);
+        else
+            role_prod_search<Cfg<MODE>::kProdWarps>(p, As, ctl, warp - kWarpProd0, lane);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpTmem) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int MODE>
+cudaError_t launch_tc(const CUtensorMap& mapX, const TcParams& p, int num_sms, cudaStream_t st) {
+    if (p.n_items <= 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(tc_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = p.n_items < num_sms ? p.n_items : num_sms;
+    tc_kernel<MODE><<<grid, Cfg<MODE>::kThreads, kSmemBytes, st>>>(mapX, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc_gemm(const CUtensorMap& mapX, const TcParams& p, int num_sms,
+                           cudaStream_t st) {
+    return launch_tc<kModeGemm>(mapX, p, num_sms, st);
+}
+cudaError_t launch_tc_search(const CUtensorMap& mapX, const TcParams& p, int num_sms,
+                             cudaStream_t st) {
+    return launch_tc<kModeSearch>(mapX, p, num_sms, st);
+}
+
+}  // namespace awq
