@@ -1,0 +1,452 @@
+#!/usr/bin/env python
+"""Benchmark of the AWQ hot path on B300.
+
+Workload (default): LLaMA-7B-shaped decode at M = 1 over the four
+projections (fused qkv 12288x4096, o 4096x4096, fused gate+up 22016x4096,
+down 4096x11008), fp16 weights ~ N(0, 0.02^2), activations ~ N(0,1) with 1%
+of input channels x20, quantised to INT4 g128 by the AWQ search on 512
+calibration tokens.  One step = the whole hot path on every projection:
+act_stats -> act_mean -> search_scale (20 alphas) -> pack_int4, then an L2
+flush, then w4a16_gemm at M = 1 on every projection.
+
+Headline ``value``: W4A16 GEMV HBM GB/s at M = 1, i.e. the algorithmic bytes
+of the four decode matmuls (packed weights + scales/zeros + x + y) over
+their CUDA-event time inside the timed steps.  ``ms_per_step`` is the whole
+step.  ``roofline`` is for the dominant kernel of the step (the fused search
+GEMM), ``roofline_gemv`` for the headline kernel.
+
+``--impl reference`` times the CPU oracle on a bounded sample of the same
+workload (the oracle is the reference implementation of this method here).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthgen as sg  # noqa: E402
+
+METRIC = "W4A16 GEMV HBM GB/s (M=1) & GEMM TFLOP/s (M≥256), % of B300 roofline"
+T_CAL = 512
+N_ALPHA = 20
+FLUSH_BYTES = 512 << 20          # > 4x the 126 MB L2
+WORKLOAD = ("LLaMA-7B-shaped decode GEMV, M=1, projections qkv 12288x4096, o 4096x4096, "
+            "gate_up 22016x4096, down 4096x11008; W ~ N(0,0.02^2) fp16, X ~ N(0,1) with 1% "
+            "channels x20; INT4 g128 via AWQ search (20 alphas) on 512 calibration tokens")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+# Per-launch DRAM traffic of the fused search kernel from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), per 2*T*N*K*n_alpha flop,
+# valid while the kernel source hash matches.
+SEARCH_TRAFFIC = None     # {"bytes_per_gflop": ..., "src_sha": ...}
+
+
+def gemv_bytes(N, K, M=1):
+    return N * K // 2 + 4 * N * (K // 128) + 2 * M * K + 2 * M * N
+
+
+def search_flop(N, K, T=T_CAL, n_alpha=N_ALPHA):
+    return 2.0 * T * N * K * n_alpha
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def src_sha(name):
+    import hashlib
+    path = os.path.join(ROOT, "weight_only_bit_stats_b300", "csrc", name)
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms while the timed region runs."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+        self.t0 = self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.p.terminate()
+        self.p.wait()
+        self.f.flush()
+        rows = []
+        for line in open(self.f.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            except ValueError:
+                continue
+            rows.append((ts, parts))
+        os.unlink(self.f.name)
+        sel = [p for ts, p in rows if self.t0 - 1 <= ts <= self.t1 + 1] or [p for _, p in rows]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(p[2]) for p in sel if p[2].replace(".", "").isdigit()]
+        mx = [float(p[3]) for p in sel if p[3].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in sel:
+            for n, v in zip(names, p[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sel)}
+
+
+# ------------------------------------------------------------- GPU arm ----
+
+def run_ours(args, rank, world):
+    import torch
+    import weight_only_bit_stats_b300 as wb
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    layer = rank            # each rank quantises and runs its own layer (weak scaling)
+    projs = []
+    for j, (name, N, K) in enumerate(sg.LLAMA7B_DECODE_PROJ):
+        W, Xc, Xm, _ = sg.layer_inputs(layer, j, N, K, T_CAL, M=1)
+        projs.append(dict(name=name, N=N, K=K, W_h=W, Xc_h=Xc, x_h=Xm))
+    for p in projs:
+        N, K = p["N"], p["K"]
+        p["W"] = torch.from_numpy(p["W_h"]).to(dev)
+        p["Xc"] = torch.from_numpy(p["Xc_h"]).to(dev)
+        p["x"] = torch.from_numpy(p["x_h"]).to(dev)
+        p["abs"] = torch.empty(K, dtype=torch.int64, device=dev)
+        p["mean"] = torch.empty(K, dtype=torch.float64, device=dev)
+        p["s"] = torch.empty(K, dtype=torch.float32, device=dev)
+        p["mse"] = torch.empty(N_ALPHA, dtype=torch.float64, device=dev)
+        p["best"] = torch.empty(1, dtype=torch.int32, device=dev)
+        p["ws"] = wb.search_workspace(N, K, T_CAL, N_ALPHA, dev)
+        p["qw"] = torch.empty((N, K // 8), dtype=torch.int32, device=dev)
+        p["sc"] = torch.empty((N, K // 128), dtype=torch.float16, device=dev)
+        p["ze"] = torch.empty((N, K // 128), dtype=torch.float16, device=dev)
+        p["y"] = torch.empty((1, N), dtype=torch.float16, device=dev)
+    flush_w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)  # noqa: F841
+    stream = torch.cuda.current_stream()
+    E = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step(ev=None):
+        for i, p in enumerate(projs):
+            if ev: ev[i][0].record(stream)
+            wb.act_stats(p["Xc"], out=p["abs"])
+            if ev: ev[i][1].record(stream)
+            wb.act_mean(p["abs"], T_CAL, out=p["mean"])
+            if ev: ev[i][2].record(stream)
+            wb.search_scale(p["W"], p["Xc"], p["mean"], workspace=p["ws"],
+                            out=(p["s"], p["mse"], p["best"]))
+            if ev: ev[i][3].record(stream)
+            wb.pack_int4(p["W"], p["s"], out=(p["qw"], p["sc"], p["ze"]))
+            if ev: ev[i][4].record(stream)
+        # L2 flush: write a buffer larger than L2, then read another one so the
+        # cache holds clean lines when the decode matmuls start
+        flush_w.fill_(1.0)
+        torch.sum(flush_r, dim=0, out=flush_out)
+        if ev: ev[4][0].record(stream)
+        for i, p in enumerate(projs):
+            wb.w4a16_gemm(p["x"], p["qw"], p["sc"], p["ze"], out=p["y"])
+            if ev: ev[4][i + 1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    wb.sync_status()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.3)
+    evs = [[[E() for _ in range(5)] for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = E(), E()
+    if sampler: sampler.mark_start()
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if sampler: sampler.mark_end()
+    if world > 1:
+        dist.barrier()
+    wb.sync_status()
+    total_ms = t_start.elapsed_time(t_end)
+    st = {"stats": 0.0, "mean": 0.0, "search": 0.0, "pack": 0.0, "flush": 0.0, "gemv": 0.0}
+    per_search = [0.0] * 4
+    per_gemv = [0.0] * 4
+    for k in range(args.steps):
+        e = evs[k]
+        for i in range(4):
+            st["stats"] += e[i][0].elapsed_time(e[i][1])
+            st["mean"] += e[i][1].elapsed_time(e[i][2])
+            d = e[i][2].elapsed_time(e[i][3])
+            st["search"] += d
+            per_search[i] += d
+            st["pack"] += e[i][3].elapsed_time(e[i][4])
+            g = e[4][i].elapsed_time(e[4][i + 1])
+            st["gemv"] += g
+            per_gemv[i] += g
+        st["flush"] += e[3][4].elapsed_time(e[4][0])
+    clocks = sampler.stop() if sampler else None
+
+    # max over ranks of the timed region and the GEMV segment
+    gemv_ms = st["gemv"]
+    if world > 1:
+        t = torch.tensor([total_ms, gemv_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, gemv_ms = float(t[0]), float(t[1])
+    bytes_step = sum(gemv_bytes(p["N"], p["K"]) for p in projs)
+    flop_step = sum(search_flop(p["N"], p["K"]) for p in projs)
+    value = world * bytes_step * args.steps / (gemv_ms * 1e-3) / 1e9
+    peaks, peak_src = load_peaks()
+    search_tf = flop_step * args.steps / (st["search"] * 1e-3) / 1e12
+    gemv_gbs = bytes_step * args.steps / (st["gemv"] * 1e-3) / 1e9
+    traffic = None
+    if SEARCH_TRAFFIC and SEARCH_TRAFFIC.get("src_sha") == src_sha("tc.cu"):
+        traffic = SEARCH_TRAFFIC["bytes_per_gflop"] * flop_step / 4 / 1e9
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": 1, "calibration_tokens": T_CAL, "alphas": N_ALPHA,
+                   "l2": "flushed every step before the decode matmuls (512 MiB write + 512 MiB "
+                         "read); the step's fp16 weights (405 MB) also exceed L2",
+                   "parallelism": f"replicas x{world} (one layer per GPU, no collective)",
+                   "value_basis": "decode-matmul algorithmic bytes / CUDA-event time of the "
+                                  "decode segment of each timed step"},
+        "roofline": {"kernel": "tc_kernel<search> (fused fake-quant + tcgen05 GEMM + MSE)",
+                     "bound": "tensor", "achieved": round(search_tf, 2),
+                     "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": round(search_tf / peaks["bf16_tflops_sustained"], 4),
+                     "peak_source": f"{peak_src} bf16 dense sustained (fp16 nominal = bf16)",
+                     "traffic": traffic,
+                     "timing": "CUDA events around each awq_search_scale call (includes its "
+                               "candidate-scale and final-reduction kernels)"},
+        "roofline_gemv": {"kernel": "gemv_w4a16_kernel<1>", "bound": "hbm",
+                          "achieved": round(gemv_gbs, 1), "peak": peaks["hbm_gbs"],
+                          "unit": "GB/s", "frac": round(gemv_gbs / peaks["hbm_gbs"], 4),
+                          "peak_source": f"{peak_src} copy bandwidth"},
+        "stages_ms_per_step": {k: round(v / args.steps, 4) for k, v in st.items()},
+        "per_projection_ms": {p["name"]: {"search": round(per_search[i] / args.steps, 4),
+                                          "gemv": round(per_gemv[i] / args.steps, 5)}
+                              for i, p in enumerate(projs)},
+        "gpu_launches": args.steps * 4 * 8,
+        "clocks": clocks,
+    }
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(args, projs, dev, stream, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args, budget_s=args.cpu_budget, projs=projs)
+    return out
+
+
+def run_e2e(args, projs, dev, stream, world):
+    """Same step through the public API from pinned HOST buffers: every
+    step copies its inputs host->device and its results device->host."""
+    import torch
+    import weight_only_bit_stats_b300 as wb
+    h2d = d2h = 0
+    for p in projs:
+        p["W_pin"] = torch.from_numpy(p["W_h"]).pin_memory()
+        p["Xc_pin"] = torch.from_numpy(p["Xc_h"]).pin_memory()
+        p["x_pin"] = torch.from_numpy(p["x_h"]).pin_memory()
+        p["out_pin"] = [torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                        for t in (p["qw"], p["sc"], p["ze"], p["s"], p["best"], p["y"])]
+        h2d += p["W_pin"].nbytes + p["Xc_pin"].nbytes + p["x_pin"].nbytes
+        d2h += sum(t.nbytes for t in p["out_pin"])
+
+    def step():
+        for p in projs:
+            p["W"].copy_(p["W_pin"], non_blocking=True)
+            p["Xc"].copy_(p["Xc_pin"], non_blocking=True)
+            p["x"].copy_(p["x_pin"], non_blocking=True)
+        for p in projs:
+            wb.act_stats(p["Xc"], out=p["abs"])
+            wb.act_mean(p["abs"], T_CAL, out=p["mean"])
+            wb.search_scale(p["W"], p["Xc"], p["mean"], workspace=p["ws"],
+                            out=(p["s"], p["mse"], p["best"]))
+            wb.pack_int4(p["W"], p["s"], out=(p["qw"], p["sc"], p["ze"]))
+        for p in projs:
+            wb.w4a16_gemm(p["x"], p["qw"], p["sc"], p["ze"], out=p["y"])
+        for p in projs:
+            for dst, src in zip(p["out_pin"], (p["qw"], p["sc"], p["ze"], p["s"], p["best"], p["y"])):
+                dst.copy_(src, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        step()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, 10))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t[0])
+    bytes_step = sum(gemv_bytes(p["N"], p["K"]) for p in projs)
+    return {"value": round(world * bytes_step / (ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
+            "steps": n,
+            "basis": "decode-matmul algorithmic bytes / whole-step time with host buffers "
+                     "(fp16 weights and calibration tokens in, packed weights, s, alpha, y out)"}
+
+
+# ------------------------------------------------------- oracle (CPU) arm --
+
+def oracle_step(projs, rows_search):
+    """One bounded sample of the step on the CPU oracle; returns timings."""
+    import oracle as orc
+    t = {"quant": 0.0, "gemv": 0.0}
+    for p in projs:
+        t0 = time.perf_counter()
+        m = orc.act_mean(orc.act_stats(p["Xc_h"]), T_CAL)
+        s, _, _ = orc.search_scale(p["W_h"][:rows_search], p["Xc_h"], m)
+        q = orc.pack_int4(p["W_h"], s)
+        t1 = time.perf_counter()
+        orc.w4a16_gemm(p["x_h"], *q)
+        t2 = time.perf_counter()
+        t["quant"] += t1 - t0
+        t["gemv"] += t2 - t1
+    return t
+
+
+def _oracle_projs():
+    projs = []
+    for j, (name, N, K) in enumerate(sg.LLAMA7B_DECODE_PROJ):
+        W, Xc, Xm, _ = sg.layer_inputs(0, j, N, K, T_CAL, M=1)
+        projs.append(dict(name=name, N=N, K=K, W_h=W, Xc_h=Xc, x_h=Xm))
+    return projs
+
+
+ROWS_SEARCH = 16
+SAMPLE = ("per step, each of the four projections: statistics over all 512 calibration tokens, "
+          f"the 20-alpha search on the first {ROWS_SEARCH} weight rows, INT4 pack of all rows, "
+          "and the M=1 decode matmul over all rows (value = its GB/s)")
+
+
+def cpu_baseline(args, budget_s=20.0, projs=None):
+    import oracle as orc
+    orc.build()
+    projs = projs or _oracle_projs()
+    bytes_step = sum(gemv_bytes(p["N"], p["K"]) for p in projs)
+    oracle_step(projs, ROWS_SEARCH)            # warm-up (page-in, thread pools)
+    t_gemv = t_quant = 0.0
+    n = 0
+    t_begin = time.perf_counter()
+    while n < 1 or (time.perf_counter() - t_begin < budget_s and n < 50):
+        t = oracle_step(projs, ROWS_SEARCH)
+        t_gemv += t["gemv"]
+        t_quant += t["quant"]
+        n += 1
+    return {"value": round(bytes_step * n / t_gemv / 1e9, 4), "unit": "GB/s",
+            "cores": os.cpu_count(), "kind": "oracle", "sample": SAMPLE,
+            "steps": n, "oracle_gemv_s_per_step": round(t_gemv / n, 4),
+            "oracle_quant_s_per_step": round(t_quant / n, 4)}
+
+
+def run_reference(args):
+    import oracle as orc
+    orc.build()
+    projs = _oracle_projs()
+    bytes_step = sum(gemv_bytes(p["N"], p["K"]) for p in projs)
+    for _ in range(args.warmup):
+        oracle_step(projs, ROWS_SEARCH)
+    t_gemv = t_quant = 0.0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        t = oracle_step(projs, ROWS_SEARCH)
+        t_gemv += t["gemv"]
+        t_quant += t["quant"]
+    wall = time.perf_counter() - t0
+    value = bytes_step * args.steps / t_gemv / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(wall / args.steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": 1, "calibration_tokens": T_CAL,
+                       "alphas": N_ALPHA},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": SAMPLE},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "oracle_quant_s_per_step": round(t_quant / args.steps, 4)}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    out = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

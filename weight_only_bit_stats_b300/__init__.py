@@ -104,23 +104,30 @@ def _ld(t: torch.Tensor) -> int:
     return t.stride(0) if t.dim() == 2 else t.shape[-1]
 
 
-def act_stats(X: torch.Tensor, abs_sum: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+def act_stats(X: torch.Tensor, abs_sum: torch.Tensor | None = None, out: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
     """Exact per-channel sum of |x| * 2^24 (int64 [K]).  With ``abs_sum``
-    given, this batch is added to it (streamed calibration)."""
+    given, this batch is added to it (streamed calibration); otherwise the
+    sums are written to ``out`` (or a new tensor)."""
     _dev(X, torch.float16, "X")
     T, K = X.shape
     acc = abs_sum is not None
-    out = abs_sum if acc else torch.empty(K, dtype=torch.int64, device=X.device)
+    if acc:
+        out = abs_sum
+    elif out is None:
+        out = torch.empty(K, dtype=torch.int64, device=X.device)
     _dev(out, torch.int64, "abs_sum")
     _check(lib().awq_act_stats(X.data_ptr(), T, K, _ld(X), int(acc), out.data_ptr(),
                                _stream(stream)), "awq_act_stats")
     return out
 
 
-def act_mean(abs_sum: torch.Tensor, n_tokens: int, stream=None) -> torch.Tensor:
+def act_mean(abs_sum: torch.Tensor, n_tokens: int, out: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
     """mean |x| per channel, fp64 [K]."""
     _dev(abs_sum, torch.int64, "abs_sum")
-    out = torch.empty(abs_sum.shape[0], dtype=torch.float64, device=abs_sum.device)
+    if out is None:
+        out = torch.empty(abs_sum.shape[0], dtype=torch.float64, device=abs_sum.device)
     _check(lib().awq_act_mean(abs_sum.data_ptr(), int(n_tokens), abs_sum.shape[0], out.data_ptr(),
                               _stream(stream)), "awq_act_mean")
     return out
@@ -151,7 +158,7 @@ def search_workspace(N: int, K: int, T: int, n_alpha: int, device) -> torch.Tens
 
 def search_scale(W: torch.Tensor, Xcal: torch.Tensor, mean_abs: torch.Tensor, alphas=ALPHA_GRID,
                  workspace: torch.Tensor | None = None, return_candidates: bool = False,
-                 stream=None):
+                 out=None, stream=None):
     """alpha grid search.  Returns ``(s fp32 [K], mse fp64 [n_alpha],
     best int32 [1])`` (+ all candidate scales [n_alpha, K] when
     ``return_candidates``), all on the device."""
@@ -162,9 +169,12 @@ def search_scale(W: torch.Tensor, Xcal: torch.Tensor, mean_abs: torch.Tensor, al
     T = Xcal.shape[0]
     arr, n = _alphas(alphas)
     dev = W.device
-    s = torch.empty(K, dtype=torch.float32, device=dev)
-    mse = torch.empty(n, dtype=torch.float64, device=dev)
-    best = torch.empty(1, dtype=torch.int32, device=dev)
+    if out is not None:
+        s, mse, best = out
+    else:
+        s = torch.empty(K, dtype=torch.float32, device=dev)
+        mse = torch.empty(n, dtype=torch.float64, device=dev)
+        best = torch.empty(1, dtype=torch.int32, device=dev)
     cands = torch.empty((n, K), dtype=torch.float32, device=dev) if return_candidates else None
     if workspace is None:
         workspace = search_workspace(N, K, T, n, dev)

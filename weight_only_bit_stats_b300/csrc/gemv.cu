@@ -78,11 +78,12 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Shared memory: activations of this CTA's K range, per token a row of
-// ng*256 + 64 bytes (padding keeps the 16-byte fragment reads of a quarter
-// warp on distinct banks).  Within a group the 8-element chunk of physical
-// k = 32 t + 8 i is stored at chunk position 4 i + t, its elements in the
-// order (0,4,1,5,2,6,3,7).  Then the partial-sum tile [64 rows][M].
+// Shared memory: the partial-sum tile [64 rows][M] fp32, then the
+// activations of this CTA's K range, per token a row of ng*256 + 64 bytes
+// (padding keeps the 16-byte fragment reads of a quarter warp on distinct
+// banks).  Within a group the 8-element chunk of physical k = 32 t + 8 i is
+// stored at chunk position 4 i + t, its elements in the order
+// (0,4,1,5,2,6,3,7).
 template <int NB>
 __global__ void __launch_bounds__(kGemvWarps * 32)
     gemv_w4a16_kernel(GemvParams p, int cs) {
@@ -93,8 +94,10 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
     const int ng = ge - gs;
     const int M = p.M;
     const int64_t row_stride = (int64_t)ng * 256 + 64;   // bytes per token row
-    uint8_t* xs = smem;
-    float* part = reinterpret_cast<float*>(smem + (size_t)M * row_stride);
+    // the partial-sum tile sits at offset 0 so that it has the same address
+    // in every CTA of the cluster (their K ranges, hence xs sizes, differ)
+    float* part = reinterpret_cast<float*>(smem);
+    uint8_t* xs = smem + (size_t)kGemvRows * M * 4;
 
     // ---- stage X[:, gs*128 .. ge*128) with the fragment permutation ----
     const int chunks = M * ng * 16;
