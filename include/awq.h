@@ -125,6 +125,25 @@ awq_status awq_search_scale(const uint16_t* W, int64_t N, int64_t K, int64_t ldw
                             awq_stream_t stream);
 size_t awq_search_workspace_size(int64_t N, int64_t K, int64_t T, int n_alpha);
 
+/* ---- alpha search without any device allocation ---------------------------
+ * No counterpart on the AWQ pages: an allocation-free variant of
+ * awq_search_scale for callers that cannot allocate device memory (plug-ins
+ * of a host program that owns the whole device memory pool; loops that must
+ * avoid cudaMalloc because it can synchronise the device).  Same arguments
+ * and results as awq_search_scale without the workspace: the scratch is a
+ * library-owned device array of AWQ_SEARCH_NOALLOC_SCRATCH_BYTES that every
+ * GPU loading the library holds until the process exits.  Problems whose
+ * awq_search_workspace_size() exceeds that size are refused with
+ * AWQ_ERR_WORKSPACE.  The first call on a device looks up the array's device
+ * address (make that first call before any stream capture).  All calls share
+ * the array: calls that overlap on the GPU race. */
+#define AWQ_SEARCH_NOALLOC_SCRATCH_BYTES (16u << 20)
+awq_status awq_search_scale_noalloc(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                                    const uint16_t* Xcal, int64_t T, int64_t ldx,
+                                    const double* mean_abs, const double* alphas, int n_alpha,
+                                    int group, float* s_out, double* mse_out, int32_t* best_idx,
+                                    float* s_alpha_out, awq_stream_t stream);
+
 /* ---- step: INT4 packing --------------------------------------------------
  * Low-bit weights (third paragraph: "every weight stays in low bits"; last
  * paragraph: 4 bits).  Per row n and group g of 128 input channels:

@@ -53,6 +53,8 @@ SIGNATURES = (
     ("awq_search_scale", _int, [_p, _i64, _i64, _i64, _p, _i64, _i64, _p, _p, _int, _int, _p, _p,
                                 _p, _p, _p, _sz, _p]),
     ("awq_search_workspace_size", _sz, [_i64, _i64, _i64, _int]),
+    ("awq_search_scale_noalloc", _int, [_p, _i64, _i64, _i64, _p, _i64, _i64, _p, _p, _int, _int,
+                                        _p, _p, _p, _p, _p]),
     ("awq_pack_int4", _int, [_p, _i64, _i64, _i64, _p, _int, _p, _p, _p, _p]),
     ("w4a16_gemm", _int, [_p, _i64, _i64, _i64, _p, _p, _p, _i64, _int, _p, _i64, _p, _sz, _p]),
     ("w4a16_gemm_workspace_size", _sz, [_i64, _i64, _i64]),

@@ -112,6 +112,12 @@ SearchWs search_ws(int64_t N, int64_t K, int64_t T, int n_alpha) {
 
 }  // namespace
 
+namespace awq {
+// Lets other translation units of the library report an error message
+// through awq_last_error_string().
+awq_status report_error(awq_status code, const char* msg) { return fail(code, msg); }
+}  // namespace awq
+
 extern "C" {
 
 int awq_version(void) { return 100; }
