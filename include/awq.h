@@ -7,7 +7,7 @@
  * s leaves a layer's output unchanged while shrinking that channel's relative
  * rounding error; s is the channel's average activation magnitude raised to a
  * power alpha, and alpha comes from a quick grid search on a small
- * calibration set; every weight stays in low bits.  Sixth paragraph: only
+ * calibration set; every weight stays in low bits.  Seventh paragraph: only
  * activation statistics are collected.  First paragraph: decoding reads
  * every weight once per step and is memory-bound, so 4-bit weights cut its
  * traffic about 4x.  The OpenAlex record of the same title (abstract):
@@ -65,7 +65,7 @@ typedef struct CUstream_st* awq_stream_t;
 
 /* ---- step: calibration statistics ---------------------------------------
  * Per-input-channel sum of |x| over calibration tokens (the pages' "average
- * activation magnitude", third paragraph; statistics only, sixth paragraph).
+ * activation magnitude", third paragraph; statistics only, seventh paragraph).
  *   X            [T, K] fp16, leading dimension ldx (>= K, multiple of 8),
  *                16-byte aligned; K % 8 == 0.
  *   accumulate   0: abs_sum_q24 is overwritten; 1: this batch is added to

@@ -13,7 +13,7 @@ numpy's fp64 matmul as a library step on the exact fp64 operands.
 Method source: "AWQ: Activation-aware Weight Quantization for On-Device LLM
 Compression and Acceleration" (fdeinterviews.com/papers/awq), third
 paragraph (scaling trick, s = average activation magnitude ** alpha, alpha
-by grid search on a calibration set, every weight in low bits), sixth
+by grid search on a calibration set, every weight in low bits), seventh
 paragraph (only activation statistics are collected), last paragraph
 (4 bits).  Group size 128, asymmetric fp16 scale/zero, mean |x|, output MSE
 and the 20-point alpha grid are the workload definition, not the pages'.

@@ -11,7 +11,7 @@
  *     a weight channel by s > 1 and divide its input by s; s is each channel's
  *     average activation magnitude raised to a power alpha; alpha comes from a
  *     quick grid search on a small calibration set; every weight stays in low
- *     bits.  Sixth paragraph: only activation statistics are collected.
+ *     bits.  Seventh paragraph: only activation statistics are collected.
  *     Last paragraph: 4 bits is the default.
  *   - Group size 128, asymmetric levels 0..15 with an fp16 scale and fp16
  *     zero-point per group, 8 nibbles per uint32, mean |x| as the average

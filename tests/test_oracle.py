@@ -107,7 +107,7 @@ def test_act_stats_bruteforce_fractions(oracle_mod):
 
 
 def test_act_stats_order_independent_and_streamed(oracle_mod):
-    """Only statistics are collected (pages, sixth paragraph): permuting the
+    """Only statistics are collected (pages, seventh paragraph): permuting the
     tokens or splitting them into streamed batches changes nothing."""
     _, X, _, _ = sg.layer_inputs(0, 1, 8, 256, 300)
     a = oracle_mod.act_stats(X)

@@ -1,6 +1,6 @@
 // Calibration statistics: per-input-channel sum of |x| (the pages' "average
 // activation magnitude" of "AWQ: Activation-aware Weight Quantization ...",
-// third paragraph; statistics only, sixth paragraph).
+// third paragraph; statistics only, seventh paragraph).
 //
 // Every finite fp16 value is an integer multiple of 2^-24 below 2^16, so
 // |x| * 2^24 is an integer below 2^40 and the per-channel sum is accumulated
