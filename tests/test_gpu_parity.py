@@ -296,3 +296,28 @@ def test_llama70b_prefill_sampled(wb, orc, M):
         ref = orc.w4a16_pairs(Xm, rq, rs, rz, ms, ns)
         got = y[ms, ns].astype(np.float64)
         assert rel_err(got, ref) <= GEMM_TOL, (name, M)
+
+
+def test_decode_tiny_n(wb, orc):
+    """N = 8: a single 16-row slab whose upper half lies outside the matrix."""
+    for M in (1, 16):
+        _gemm_check(wb, orc, 8, 256, M, seed=5)
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_decode_long_k_sampled(wb, orc, M):
+    """LLaMA-70B-shaped down projection (8192 x 28672) at decode sizes: every
+    token of 1024 sampled output columns against the fp64 oracle."""
+    rng = np.random.default_rng(100 + M)
+    W, _, Xm, _ = sg.layer_inputs(2, 1, 8192, 28672, 0, M=M, sigma=0.015)
+    qw, sc, ze = wb.pack_int4(dev(W))
+    del W
+    Y = torch.full((M, 8192), float("nan"), dtype=torch.float16, device="cuda")
+    wb.w4a16_gemm(dev(Xm), qw, sc, ze, out=Y)
+    y = host(Y)
+    assert np.all(np.isfinite(y))
+    cols = rng.choice(8192, 1024, replace=False)
+    ms = np.repeat(np.arange(M), cols.size)
+    ns = np.tile(cols, M)
+    ref = orc.w4a16_pairs(Xm, u32(qw), u16(sc), u16(ze), ms, ns)
+    assert rel_err(y[ms, ns].astype(np.float64), ref) <= GEMM_TOL

@@ -67,7 +67,7 @@ awq_status device_info(DevInfo** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-awq_status make_act_map(CUtensorMap* map, const uint16_t* X, int64_t rows, int64_t K, int64_t ld) {
+bool load_encoder() {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -76,7 +76,13 @@ awq_status make_act_map(CUtensorMap* map, const uint16_t* X, int64_t rows, int64
             q == cudaDriverEntryPointSuccess)
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     });
-    if (!g_encode) return fail(AWQ_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    return g_encode != nullptr;
+}
+
+// Activations [rows, K] fp16 for the tensor-core kernels: 128-byte swizzled
+// boxes of 64 k x kTcTokens rows.
+awq_status make_act_map(CUtensorMap* map, const uint16_t* X, int64_t rows, int64_t K, int64_t ld) {
+    if (!load_encoder()) return fail(AWQ_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
     cuuint32_t box[2] = {64, (cuuint32_t)awq::kTcTokens};
@@ -86,6 +92,23 @@ awq_status make_act_map(CUtensorMap* map, const uint16_t* X, int64_t rows, int64
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(AWQ_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    return AWQ_OK;
+}
+
+// Packed weights [N, K/8] uint32 for the decode kernel: unswizzled boxes of
+// 80 words (five groups of 128 nibbles) x 16 rows, landing as
+// [16 rows][320 B].
+awq_status make_qweight_map(CUtensorMap* map, const uint32_t* qw, int64_t N, int64_t K) {
+    if (!load_encoder()) return fail(AWQ_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)N};
+    cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+    cuuint32_t box[2] = {80, 16};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(qw), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(AWQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (qweight)");
     return AWQ_OK;
 }
 
@@ -316,11 +339,12 @@ awq_status w4a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx, cons
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e;
     if (M <= 16) {
-        // the staged activations of one CTA must fit in shared memory
-        if (M * ((K / AWQ_GROUP + 7) / 8 * 256 + 64) + 64 * M * 4 > 200 * 1024)
-            return fail(AWQ_ERR_SHAPE, "w4a16_gemm: K too large for the decode kernel");
-        awq::GemvParams p = {X, ldx, (int)M, qweight, scales, zeros, N, K, (int)(K / AWQ_GROUP), Y, ldy};
-        e = awq::launch_gemv(p, d->num_sms, st);
+        CUtensorMap map;
+        s = make_qweight_map(&map, qweight, N, K);
+        if (s) return s;
+        awq::GemvParams p = {X, ldx, (int)M, qweight, scales, zeros, N, K, (int)(K / AWQ_GROUP),
+                             Y, ldy, d->status};
+        e = awq::launch_gemv(map, p, d->num_sms, st);
     } else {
         CUtensorMap map;
         s = make_act_map(&map, X, M, K, ldx);

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace awq {
 
 constexpr int kGroup = 128;
@@ -42,9 +44,9 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // ---------------------------------------------------------------------------
-// INT4 group quantiser (asymmetric, group of 128 = one warp x 4 elements).
+// INT4 group quantiser (asymmetric, group of 128).
 //
-// For one row-group with scaled weights w' (each lane holds 4 of the 128):
+// For one row-group with scaled weights w':
 //   lo, hi = min, max of w'
 //   scale  = fp16_rn(max(fp32(fp32(hi - lo) / 15), 2^-14))
 //   z      = clamp(rint(fp32(-lo / scale)), 0, 15)
@@ -52,16 +54,43 @@ __device__ __forceinline__ float warp_max(float v) {
 // Every rounding is a single IEEE fp32 operation written as an _rn
 // intrinsic, so no FMA contraction can change a level.
 // ---------------------------------------------------------------------------
+
+// rint(x), ties to even, for |x| < 2^22: x + 1.5*2^23 lies in [2^23, 2^24)
+// where fp32 values are the integers, so the sum is x rounded to an integer
+// (ties to even, as 1.5*2^23 is even), and subtracting the constant is exact.
+// For larger |x| the result is off by at most 2 (callers only use it there
+// after a check that sends such x to the exact path).
+__device__ __forceinline__ float rint_small(float x) {
+    const float c = 12582912.0f;   // 1.5 * 2^23
+    return __fsub_rn(__fadd_rn(x, c), c);
+}
+
+// rint(fp32(a / b)) exactly, given rb = fp32(1 / b) correctly rounded.
+// t0 = fp32(a * rb) carries two rounding errors of at most 2^-24 relative
+// each, so |t0 - fp32(a / b)| <= 3 * 2^-24 |t0| (to first order).  When no
+// half-integer lies within 2^-21 |t0| of t0 -- margin 2.6x that bound, and
+// the margin itself is computed exactly for |t0| >= 1/4 (Sterbenz), while
+// below 1/4 both roundings give 0 -- rint(t0) is rint(fp32(a / b)).
+// Otherwise (near a tie, |t0| >= 2^22, Inf, NaN) the quotient is formed by
+// IEEE division.  The fast path uses no XU instruction.
+__device__ __forceinline__ float rint_quot(float a, float b, float rb) {
+    const float t0 = __fmul_rn(a, rb);
+    const float rt = rint_small(t0);
+    const float margin = __fsub_rn(0.5f, fabsf(__fsub_rn(t0, rt)));
+    if (margin > __fmul_rn(fabsf(t0), 4.76837158203125e-07f)) return rt;   // 2^-21
+    return rintf(__fdiv_rn(a, b));
+}
+
 struct GroupQuant {
     float scale;    // exact value of the fp16 scale
+    float rcp;      // fp32(1 / scale), correctly rounded
     float zf;       // zero-point, an integer 0..15
     __half scale_h;
     bool finite;    // false when the fp16 scale overflowed
 };
 
-__device__ __forceinline__ GroupQuant group_quant_params(float lo_lane, float hi_lane) {
-    float lo = warp_min(lo_lane);
-    float hi = warp_max(hi_lane);
+// Group parameters from the group's min and max (already reduced).
+__device__ __forceinline__ GroupQuant group_quant_from_range(float lo, float hi) {
     GroupQuant g;
     float range = __fsub_rn(hi, lo);
     float d = __fdiv_rn(range, 15.0f);
@@ -69,15 +98,28 @@ __device__ __forceinline__ GroupQuant group_quant_params(float lo_lane, float hi
     g.scale_h = __float2half_rn(d);
     g.scale = __half2float(g.scale_h);
     g.finite = isfinite(g.scale);
+    g.rcp = __frcp_rn(g.scale);
     // the zero-point is an integer level: -0 and negatives clamp to +0
-    float z = rintf(__fdiv_rn(-lo, g.scale));
+    float z = rint_quot(-lo, g.scale, g.rcp);
     g.zf = z > 0.0f ? fminf(z, 15.0f) : 0.0f;
     return g;
 }
 
+// One warp holds a group, 4 scaled weights per lane.
+__device__ __forceinline__ GroupQuant group_quant_params(float lo_lane, float hi_lane) {
+    return group_quant_from_range(warp_min(lo_lane), warp_max(hi_lane));
+}
+
 __device__ __forceinline__ float quant_level(float wp, const GroupQuant& g) {
-    float t = __fdiv_rn(wp, g.scale);
-    return fminf(fmaxf(__fadd_rn(rintf(t), g.zf), 0.0f), 15.0f);
+    const float t = rint_quot(wp, g.scale, g.rcp);
+    return fminf(fmaxf(__fadd_rn(t, g.zf), 0.0f), 15.0f);
+}
+
+// (q - z) for a scaled weight: clamp(rint(w' / scale), -z, 15 - z), which is
+// clamp(rint(w' / scale) + z, 0, 15) - z exactly (small integers).
+__device__ __forceinline__ float quant_level_mz(float wp, float scale, float rcp, float neg_z,
+                                                float top_z) {
+    return fminf(fmaxf(rint_quot(wp, scale, rcp), neg_z), top_z);
 }
 
 // ---------------------------------------------------------------------------
@@ -148,6 +190,16 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// 3-D tiled TMA load of one box (coordinates innermost first).
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
 
@@ -245,6 +297,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Host: raise a kernel's dynamic shared-memory limit once per device.  The
+// attribute call is driver work on the launch path; repeating it per launch
+// adds host latency that a short kernel cannot hide.
+template <auto Kernel>
+inline cudaError_t smem_attr_once(int bytes) {
+    static std::atomic<unsigned long long> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+    return e;
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

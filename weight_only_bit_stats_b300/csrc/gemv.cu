@@ -2,42 +2,67 @@
 //
 // Decoding reads every weight once per step and does little arithmetic with
 // it ("AWQ: Activation-aware Weight Quantization ...", fdeinterviews.com/
-// papers/awq, first paragraph), so this kernel is built to stream the packed
-// words at HBM speed with the fewest instructions per weight:
+// papers/awq, first paragraph), so this kernel exists to stream the packed
+// words at HBM speed:
 //
-//  * Each thread issues 128-bit loads of 32 consecutive nibbles (a quarter of
-//    a group) of two weight rows; a warp covers 16 rows x one group of 128.
+//  * Persistent grid, one CTA per SM.  CTA c owns a balanced, contiguous run
+//    of 16-row slabs; its consumer warps (16 for up to 8 tokens, else 8)
+//    split the CTA's (slab, 5-group chunk) units into equal contiguous
+//    ranges, so a slab can be shared by neighbouring warps (intra-CTA
+//    split-K).
+//  * Each warp streams its units through its own ring in shared memory,
+//    filled by TMA: one 2-D box of 16 rows x 5 groups (320 contiguous bytes
+//    per row) per unit.  With a 320-byte row pitch the fragment reads of a
+//    quarter warp (two rows, 4 x 16 B each) fall on disjoint bank halves.
+//    Narrow boxes (one 64-byte group per row) are not used: on B300 the TMA
+//    then issues one small request per row and delivers only about 1 TB/s.
+//    Every warp's whole ring is requested at kernel start: 160 KB per SM in
+//    flight.
 //  * Nibbles become exact fp16 values (q - z) in registers: a LOP3 places a
 //    nibble in the mantissa of 1024.0 (or 1024 + 16 q for the high nibble of
 //    a byte), and one HSUB2 / HFMA2 removes the offset and the zero-point.
 //    (q - z) is an integer in [-15, 15], so nothing is rounded.
 //  * The products go to the tensor cores through register-sourced
 //    mma.m16n8k16 (fp16 in, fp32 accumulate), which keeps the M FMAs per
-//    weight off the FP32 pipe: with CUDA-core FMAs alone the dequantise +
-//    multiply work would cap the kernel below HBM speed.  Tensor memory and
-//    shared-memory operands (tcgen05) would add an smem round trip per
-//    weight, which costs more bandwidth than this path saves.
-//  * The MMA's k order is a permutation of the physical k order chosen so
-//    that each thread's loaded words are exactly its A-fragment; the
-//    activations are staged in shared memory under the same permutation.
+//    weight off the FP32 pipe.  The MMA's k order is a permutation of the
+//    physical k order chosen so that each thread's 16 loaded bytes of a row
+//    are exactly its A fragment; each thread reads the matching 64 bytes of
+//    activations (L1-resident) and applies the same permutation with PRMT.
 //    The group scale is applied in fp32 to the per-group partial sums.
-//  * K is split over the CTAs of a thread-block cluster; partial sums are
-//    reduced in a fixed order through distributed shared memory, so the
-//    kernel needs no workspace and is deterministic.
-#include <cooperative_groups.h>
-
+//  * A slab owned by one warp is written straight from registers; a slab
+//    shared by several warps is reduced through shared memory in warp order.
+//    The work split depends on N and K only, so the result is deterministic
+//    and independent of M, and the kernel needs no workspace.
 #include "common.cuh"
 #include "kernels.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace awq {
 namespace {
 
-constexpr int kGemvWarps = 4;                 // 16 weight rows per warp
-constexpr int kGemvRows = 16 * kGemvWarps;    // rows per CTA
-constexpr int kGemvBatch = 4;                 // groups loaded ahead per warp
-constexpr size_t kGemvSmemMax = 200 * 1024;
+constexpr int kDecRows = 16;                        // rows per slab (MMA M)
+// Groups per ring stage.  One TMA box per stage: 16 rows x kDecChunk groups
+// (row pitch kDecChunk * 64 B in shared memory).  An odd count makes the
+// pitch an odd multiple of 64 B, so the two rows a quarter warp reads sit on
+// disjoint bank halves; wide rows keep the TMA's per-row request count low.
+constexpr int kDecChunk = 5;
+constexpr int kDecPitch = kDecChunk * 64;                     // 320 B
+constexpr int kDecStageBytes = kDecRows * kDecPitch;          // 5 KB
+static_assert(kDecChunk % 2 == 1, "row pitch must be an odd multiple of 64 bytes");
+
+// Consumer warps per CTA: 16 with a 2-stage ring each for up to 8 tokens,
+// 8 (more registers each) with a 3-stage ring for 9..16 tokens.
+template <int NW>
+struct DecCfg {
+    static constexpr int kThreads = NW * 32;
+    static constexpr int kStages = NW >= 16 ? 2 : 3;
+    static constexpr int kSlots = 2 * NW;           // partial sums: first/last slab of each warp
+    static constexpr size_t kRingBytes = (size_t)NW * kStages * kDecStageBytes;
+    static constexpr size_t kPartBytes = (size_t)kSlots * kDecRows * 16 * sizeof(float);
+    static constexpr size_t kCtlBytes = (size_t)NW * kStages * 8 + (size_t)NW * 12 + 16;
+    static constexpr size_t kSmem = 1024 + kRingBytes + kPartBytes + kCtlBytes;
+};
+static_assert(DecCfg<16>::kSmem <= 232448 && DecCfg<8>::kSmem <= 232448,
+              "decode kernel exceeds shared memory");
 
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t d;
@@ -78,205 +103,311 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Shared memory: the partial-sum tile [64 rows][M] fp32, then the
-// activations of this CTA's K range, per token a row of ng*256 + 64 bytes
-// (padding keeps the 16-byte fragment reads of a quarter warp on distinct
-// banks).  Within a group the 8-element chunk of physical k = 32 t + 8 i is
-// stored at chunk position 4 i + t, its elements in the order
-// (0,4,1,5,2,6,3,7).
-template <int NB>
-__global__ void __launch_bounds__(kGemvWarps * 32)
-    gemv_w4a16_kernel(GemvParams p, int cs) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rb = blockIdx.x / cs, split = blockIdx.x % cs;
-    const int gs = (int)((int64_t)split * p.G / cs), ge = (int)((int64_t)(split + 1) * p.G / cs);
-    const int ng = ge - gs;
-    const int M = p.M;
-    const int64_t row_stride = (int64_t)ng * 256 + 64;   // bytes per token row
-    // the partial-sum tile sits at offset 0 so that it has the same address
-    // in every CTA of the cluster (their K ranges, hence xs sizes, differ)
-    float* part = reinterpret_cast<float*>(smem);
-    uint8_t* xs = smem + (size_t)kGemvRows * M * 4;
+// 8 physical activations (x0..x7) -> the B-fragment order of the permuted k:
+// (x0,x4) (x1,x5) (x2,x6) (x3,x7).
+__device__ __forceinline__ uint4 permute_x8(uint4 v) {
+    uint4 o;
+    o.x = prmt(v.x, v.z, 0x5410);
+    o.y = prmt(v.x, v.z, 0x7632);
+    o.z = prmt(v.y, v.w, 0x5410);
+    o.w = prmt(v.y, v.w, 0x7632);
+    return o;
+}
 
-    // ---- stage X[:, gs*128 .. ge*128) with the fragment permutation ----
-    const int chunks = M * ng * 16;
-    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
-        const int m = c / (ng * 16), rem = c - m * ng * 16;
-        const int gl = rem >> 4, k8 = rem & 15;          // group, chunk within group
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-            p.X + (int64_t)m * p.ldx + (int64_t)(gs + gl) * kGroup + k8 * 8));
-        uint4 o;
-        o.x = prmt(v.x, v.z, 0x5410);    // (x0, x4)
-        o.y = prmt(v.x, v.z, 0x7632);    // (x1, x5)
-        o.z = prmt(v.y, v.w, 0x5410);    // (x2, x6)
-        o.w = prmt(v.y, v.w, 0x7632);    // (x3, x7)
-        const int t = k8 >> 2, i = k8 & 3;
-        *reinterpret_cast<uint4*>(xs + (int64_t)m * row_stride + gl * 256 + (i * 4 + t) * 16) = o;
+// Per-group operands a thread needs besides the weights: the scale and
+// zero-point of its two rows, and its 64 bytes of each token's activations.
+template <int NB>
+struct GroupIn {
+    uint16_t sa, sb, za, zb;
+    uint4 x[NB][4];
+};
+
+template <int NB>
+__device__ __forceinline__ void load_group_in(GroupIn<NB>& in, const GemvParams& p, int64_t row_a,
+                                              int gi, int g, int t) {
+    const bool va = row_a < p.N, vb = row_a + 8 < p.N;
+    in.sa = va ? __ldg(p.scales + row_a * p.G + gi) : (uint16_t)0;
+    in.za = va ? __ldg(p.zeros + row_a * p.G + gi) : (uint16_t)0;
+    in.sb = vb ? __ldg(p.scales + (row_a + 8) * p.G + gi) : (uint16_t)0;
+    in.zb = vb ? __ldg(p.zeros + (row_a + 8) * p.G + gi) : (uint16_t)0;
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        const int tok = g + 8 * nb;
+        if (tok < p.M) {
+            const uint4* xp = reinterpret_cast<const uint4*>(p.X + (int64_t)tok * p.ldx +
+                                                             (int64_t)gi * kGroup + 32 * t);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) in.x[nb][i] = __ldg(xp + i);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) in.x[nb][i] = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+// y += scale * (X_group (q - z)^T) for one group: 8 (16 for NB = 2) MMAs in
+// four independent accumulator chains (one per packed word), added in a
+// fixed order.
+template <int NB>
+__device__ __forceinline__ void group_mma(float (&y)[NB][4], const GroupIn<NB>& in, uint4 wa,
+                                          uint4 wb) {
+    const __half za = __ushort_as_half(in.za), zb = __ushort_as_half(in.zb);
+    const __half h1024 = __float2half_rn(1024.0f), h64 = __float2half_rn(64.0f);
+    const __half2 za1024 = __half2half2(__hadd(h1024, za));
+    const __half2 zb1024 = __half2half2(__hadd(h1024, zb));
+    const __half2 zaneg = __half2half2(__hneg(__hadd(h64, za)));
+    const __half2 zbneg = __half2half2(__hneg(__hadd(h64, zb)));
+    const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
+    const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
+    float c[NB][4][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) c[nb][i][j] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t pa[4], pb[4];
+        dequant_word(wA[i], za1024, zaneg, pa);
+        dequant_word(wB[i], zb1024, zbneg, pb);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            const uint4 b = permute_x8(in.x[nb][i]);
+            mma16816(c[nb][i], pa[0], pb[0], pa[1], pb[1], b.x, b.y);
+            mma16816(c[nb][i], pa[2], pb[2], pa[3], pb[3], b.z, b.w);
+        }
+    }
+    const float fsa = __half2float(__ushort_as_half(in.sa));
+    const float fsb = __half2float(__ushort_as_half(in.sb));
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        float s[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            s[j] = (c[nb][0][j] + c[nb][1][j]) + (c[nb][2][j] + c[nb][3][j]);
+        y[nb][0] = fmaf(fsa, s[0], y[nb][0]);
+        y[nb][1] = fmaf(fsa, s[1], y[nb][1]);
+        y[nb][2] = fmaf(fsb, s[2], y[nb][2]);
+        y[nb][3] = fmaf(fsb, s[3], y[nb][3]);
+    }
+}
+
+// First unit of warp j when U units are split over NW warps (NW a power of
+// two, so the division is a shift).
+template <int NW>
+__device__ __forceinline__ int warp_lo(int U, int j) {
+    return (int)(((int64_t)j * U) / NW);
+}
+
+template <int NW>
+struct DecCtl {
+    uint64_t full[NW][DecCfg<NW>::kStages];
+    int w_lo[NW], w_hi[NW], w_first[NW];    // each warp's unit range and first slab
+    int abort;
+};
+static_assert(sizeof(DecCtl<16>) <= DecCfg<16>::kCtlBytes &&
+                  sizeof(DecCtl<8>) <= DecCfg<8>::kCtlBytes,
+              "control block does not fit its shared-memory slot");
+
+template <int NB, int NW>
+__global__ void __launch_bounds__(NW * 32, 1)
+    gemv_w4a16_kernel(const __grid_constant__ CUtensorMap mapW, const GemvParams p) {
+    using Cfg = DecCfg<NW>;
+    constexpr int kDecWarps = NW;
+    constexpr int kDecThreads = Cfg::kThreads;
+    constexpr int kDecStages = Cfg::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* ring = smem;
+    float* part = reinterpret_cast<float*>(smem + Cfg::kRingBytes);
+    DecCtl<NW>* ctl = reinterpret_cast<DecCtl<NW>*>(smem + Cfg::kRingBytes + Cfg::kPartBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+
+    // ---- work split: slabs over CTAs, (slab, chunk) units over warps ----
+    // CTA-local unit indices fit in 32 bits (checked on the host), and the
+    // loop walks (slab, chunk) incrementally: no 64-bit division anywhere.
+    const int n_slabs = (int)((p.N + kDecRows - 1) / kDecRows);
+    const int CG = (p.G + kDecChunk - 1) / kDecChunk;
+    const int s0 = (int)((int64_t)blockIdx.x * n_slabs / gridDim.x);
+    const int s1 = (int)((int64_t)(blockIdx.x + 1) * n_slabs / gridDim.x);
+    const int U = (s1 - s0) * CG;
+    const int u_lo = warp_lo<NW>(U, warp), u_hi = warp_lo<NW>(U, warp + 1);
+    const int n_my = u_hi - u_lo;
+    const int first_sl = u_lo / CG;                     // this warp's first CTA-local slab
+    uint8_t* my_ring = ring + (size_t)warp * kDecStages * kDecStageBytes;
+
+    if (lane == 0) {
+        for (int s = 0; s < kDecStages; ++s) mbar_init(&ctl->full[warp][s], 1);
+        fence_mbar_init();
+        ctl->w_lo[warp] = u_lo;
+        ctl->w_hi[warp] = u_hi;
+        ctl->w_first[warp] = first_sl;
+    }
+    if (threadIdx.x == 0) {
+        ctl->abort = 0;
+        tma_prefetch_desc(&mapW);
     }
     __syncthreads();
 
-    // ---- main loop: this warp's 16 rows over the CTA's groups ----
-    const int g = lane >> 2, t = lane & 3;
-    const int64_t n_base = (int64_t)rb * kGemvRows + warp * 16;
-    const int64_t ra = n_base + g, rbw = n_base + g + 8;
-    const bool va = ra < p.N, vb = rbw < p.N;
-    const int64_t wstride = p.K / 8;     // words per row
-    const uint32_t* qa = p.qw + (va ? ra : 0) * wstride + 4 * t;
-    const uint32_t* qb = p.qw + (vb ? rbw : 0) * wstride + 4 * t;
-    const uint16_t* sa_p = p.scales + (va ? ra : 0) * p.G;
-    const uint16_t* sb_p = p.scales + (vb ? rbw : 0) * p.G;
-    const uint16_t* za_p = p.zeros + (va ? ra : 0) * p.G;
-    const uint16_t* zb_p = p.zeros + (vb ? rbw : 0) * p.G;
-    // activation fragments: token columns g (and g + 8)
-    const bool tok0 = g < M, tok1 = (NB == 2) && (g + 8 < M);
-    const uint8_t* x0 = xs + (int64_t)(tok0 ? g : 0) * row_stride + t * 16;
-    const uint8_t* x1 = xs + (int64_t)(tok1 ? g + 8 : 0) * row_stride + t * 16;
+    // lane 0: request unit u (CTA-local) into ring stage s: one box of 16
+    // rows x kDecChunk groups (groups past K and rows past N are zero-filled
+    // and still count toward the box's bytes)
+    auto issue = [&](int u, int s) {
+        const int sl = u / CG;
+        const int ch = u - sl * CG;
+        uint64_t* bar = &ctl->full[warp][s];
+        mbar_arrive_expect_tx(bar, (uint32_t)kDecStageBytes);
+        tma_load_2d(my_ring + (size_t)s * kDecStageBytes, &mapW, bar, ch * kDecChunk * 16,
+                    (s0 + sl) * kDecRows);
+    };
+    if (lane == 0)
+        for (int i = 0; i < kDecStages && i < n_my; ++i) issue(u_lo + i, i);
+    __syncwarp();
+
+    // write a finished slab: straight to Y when this warp owns the whole
+    // slab, else into this warp's first/last partial slot
+    auto flush = [&](int sl, const float (&y)[NB][4]) {
+        const bool owned = sl * CG >= u_lo && (sl + 1) * CG <= u_hi;
+        const int64_t row0 = (int64_t)(s0 + sl) * kDecRows;
+        if (owned) {
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int tok = nb * 8 + 2 * t + (j & 1);
+                    const int64_t row = row0 + g + ((j < 2) ? 0 : 8);
+                    if (tok < p.M && row < p.N)
+                        p.Y[(int64_t)tok * p.ldy + row] =
+                            __half_as_ushort(__float2half_rn(y[nb][j]));
+                }
+        } else {
+            const int slot = 2 * warp + (sl == first_sl ? 0 : 1);
+            float* dst = part + (size_t)slot * kDecRows * 16;
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int tok = nb * 8 + 2 * t + (j & 1);
+                    const int rl = g + ((j < 2) ? 0 : 8);
+                    dst[rl * 16 + tok] = y[nb][j];
+                }
+        }
+    };
 
     float y[NB][4];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
         for (int j = 0; j < 4; ++j) y[nb][j] = 0.0f;
-
-    for (int gb = gs; gb < ge; gb += kGemvBatch) {
-        uint4 wa[kGemvBatch], wb[kGemvBatch];
-        uint16_t sca[kGemvBatch], scb[kGemvBatch], zea[kGemvBatch], zeb[kGemvBatch];
-#pragma unroll
-        for (int u = 0; u < kGemvBatch; ++u) {
-            const int gi = gb + u;
-            if (gi < ge) {
-                wa[u] = va ? __ldg(reinterpret_cast<const uint4*>(qa + (int64_t)gi * 16))
-                           : make_uint4(0, 0, 0, 0);
-                wb[u] = vb ? __ldg(reinterpret_cast<const uint4*>(qb + (int64_t)gi * 16))
-                           : make_uint4(0, 0, 0, 0);
-                sca[u] = __ldg(sa_p + gi);
-                scb[u] = __ldg(sb_p + gi);
-                zea[u] = __ldg(za_p + gi);
-                zeb[u] = __ldg(zb_p + gi);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kGemvBatch; ++u) {
-            const int gi = gb + u;
-            if (gi >= ge) break;
-            const __half za = __ushort_as_half(zea[u]), zb = __ushort_as_half(zeb[u]);
-            const __half h1024 = __float2half_rn(1024.0f), h64 = __float2half_rn(64.0f);
-            const __half2 za1024 = __half2half2(__hadd(h1024, za));
-            const __half2 zb1024 = __half2half2(__hadd(h1024, zb));
-            const __half2 zaneg = __half2half2(__hneg(__hadd(h64, za)));
-            const __half2 zbneg = __half2half2(__hneg(__hadd(h64, zb)));
-            const uint32_t wA[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};
-            const uint32_t wB[4] = {wb[u].x, wb[u].y, wb[u].z, wb[u].w};
-            const int64_t goff = (int64_t)(gi - gs) * 256;
-            float c[NB][4];
+    int cur = -1;
+    int sl = first_sl, ch = u_lo - first_sl * CG;       // (slab, chunk) of unit u_lo + i
+    int i = 0;
+    bool ok = true;
+    for (; i < n_my; ++i) {
+        if (sl != cur) {
+            if (cur >= 0) flush(cur, y);
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) c[nb][j] = 0.0f;
+                for (int j = 0; j < 4; ++j) y[nb][j] = 0.0f;
+            cur = sl;
+        }
+        const int64_t row_a = (int64_t)(s0 + sl) * kDecRows + g;
+        const int gb = ch * kDecChunk, ge = min(p.G, gb + kDecChunk);
+        // operands of the chunk's first group go out before the wait
+        GroupIn<NB> nxt;
+        load_group_in<NB>(nxt, p, row_a, gb, g, t);
+        const int s = i % kDecStages;
+        if (!mbar_wait(&ctl->full[warp][s], (uint32_t)(i / kDecStages) & 1u, &ctl->abort,
+                       p.status)) {
+            ok = false;
+            break;
+        }
+        const uint8_t* box = my_ring + (size_t)s * kDecStageBytes;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                uint32_t pa[4], pb[4];
-                dequant_word(wA[i], za1024, zaneg, pa);
-                dequant_word(wB[i], zb1024, zbneg, pb);
-                uint4 b0 = tok0 ? *reinterpret_cast<const uint4*>(x0 + goff + i * 64)
-                                : make_uint4(0, 0, 0, 0);
-                mma16816(c[0], pa[0], pb[0], pa[1], pb[1], b0.x, b0.y);
-                mma16816(c[0], pa[2], pb[2], pa[3], pb[3], b0.z, b0.w);
-                if (NB == 2) {
-                    uint4 b1 = tok1 ? *reinterpret_cast<const uint4*>(x1 + goff + i * 64)
-                                    : make_uint4(0, 0, 0, 0);
-                    mma16816(c[NB - 1], pa[0], pb[0], pa[1], pb[1], b1.x, b1.y);
-                    mma16816(c[NB - 1], pa[2], pb[2], pa[3], pb[3], b1.z, b1.w);
-                }
-            }
-            const float fsa = __half2float(__ushort_as_half(sca[u]));
-            const float fsb = __half2float(__ushort_as_half(scb[u]));
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-                y[nb][0] = fmaf(fsa, c[nb][0], y[nb][0]);
-                y[nb][1] = fmaf(fsa, c[nb][1], y[nb][1]);
-                y[nb][2] = fmaf(fsb, c[nb][2], y[nb][2]);
-                y[nb][3] = fmaf(fsb, c[nb][3], y[nb][3]);
+        for (int jg = 0; jg < kDecChunk; ++jg) {
+            const int gi = gb + jg;
+            if (gi < ge) {
+                const GroupIn<NB> in = nxt;
+                if (gi + 1 < ge) load_group_in<NB>(nxt, p, row_a, gi + 1, g, t);
+                const uint8_t* gbox = box + jg * 64 + t * 16;
+                const uint4 wa = *reinterpret_cast<const uint4*>(gbox + g * kDecPitch);
+                const uint4 wb = *reinterpret_cast<const uint4*>(gbox + (g + 8) * kDecPitch);
+                group_mma<NB>(y, in, wa, wb);
             }
         }
+        __syncwarp();
+        if (lane == 0 && i + kDecStages < n_my) {
+            // the warp's reads of this stage are done; TMA may overwrite it
+            fence_proxy_async_smem();
+            issue(u_lo + i + kDecStages, s);
+        }
+        if (++ch == CG) {
+            ch = 0;
+            ++sl;
+        }
     }
+    if (ok && cur >= 0) flush(cur, y);
+    if (!ok && lane == 0) {
+        // bounded drain of the copies this warp still has in flight
+        for (int k = i; k < n_my && k < i + kDecStages; ++k) {
+            const unsigned long long t0 = globaltimer_ns();
+            while (!mbar_try_wait(&ctl->full[warp][k % kDecStages], (uint32_t)(k / kDecStages) & 1u))
+                if (globaltimer_ns() - t0 > 100000000ull) break;
+        }
+    }
+    __syncthreads();
+    if (ctl->abort) return;
 
-    // ---- write out: C fragment = rows (g, g+8) x tokens (2t, 2t+1) (+8 nb) ----
-    if (cs == 1) {
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int tok = nb * 8 + 2 * t + (j & 1);
-                const int64_t row = (j < 2) ? ra : rbw;
-                if (tok < M && row < p.N)
-                    p.Y[(int64_t)tok * p.ldy + row] = __half_as_ushort(__float2half_rn(y[nb][j]));
+    // ---- slabs shared by several warps: add the partials in warp order ----
+    // The slab holding warp b's first unit is shared when that unit is not
+    // the slab's first; the lowest such b reduces it, all such slabs at once.
+    if (warp >= 1 && u_lo < U && u_lo % CG != 0) {
+        const int rsl = u_lo / CG;
+        if (ctl->w_lo[warp - 1] <= rsl * CG) {
+            const int64_t row0 = (int64_t)(s0 + rsl) * kDecRows;
+            for (int e = lane; e < kDecRows * p.M; e += 32) {
+                const int r = e / p.M, m = e - r * p.M;
+                float acc = 0.0f;
+                for (int j = 0; j < NW; ++j) {
+                    const int lo = ctl->w_lo[j], hi = ctl->w_hi[j];
+                    if (hi <= lo || hi <= rsl * CG || lo >= (rsl + 1) * CG) continue;
+                    const int slot = 2 * j + (ctl->w_first[j] == rsl ? 0 : 1);
+                    acc += part[(slot * kDecRows + r) * 16 + m];
+                }
+                const int64_t row = row0 + r;
+                if (row < p.N)
+                    p.Y[(int64_t)m * p.ldy + row] = __half_as_ushort(__float2half_rn(acc));
             }
-        return;
-    }
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int tok = nb * 8 + 2 * t + (j & 1);
-            const int rl = warp * 16 + g + ((j < 2) ? 0 : 8);
-            if (tok < M) part[rl * M + tok] = y[nb][j];
         }
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();
-    // CTA `split` reduces its share of the [64 x M] tile over all ranks, in
-    // rank order, and writes fp16.
-    const int tile = kGemvRows * M;
-    const int per = (tile + cs - 1) / cs;
-    const int e0 = split * per, e1 = min(tile, e0 + per);
-    for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
-        float acc = 0.0f;
-        for (int q = 0; q < cs; ++q) acc += cluster.map_shared_rank(part, q)[e];
-        const int rl = e / M, tok = e - rl * M;
-        const int64_t row = (int64_t)rb * kGemvRows + rl;
-        if (row < p.N) p.Y[(int64_t)tok * p.ldy + row] = __half_as_ushort(__float2half_rn(acc));
     }
-    cluster.sync();
 }
 
-template <int NB>
-cudaError_t launch_gemv_nb(const GemvParams& p, int num_sms, cudaStream_t st) {
-    const int64_t n_rb = (p.N + kGemvRows - 1) / kGemvRows;
-    auto smem_for = [&](int c) {
-        const int max_ng = (p.G + c - 1) / c;
-        return (size_t)p.M * ((size_t)max_ng * 256 + 64) + (size_t)kGemvRows * p.M * 4;
-    };
-    // split K over up to 8 CTAs: enough CTAs to fill the GPU, and few enough
-    // groups per CTA for the staged activations to fit in shared memory
-    int cs = 1;
-    while (cs < 8 && 2 * cs <= p.G && (n_rb * cs < 4LL * num_sms || smem_for(cs) > kGemvSmemMax))
-        cs *= 2;
-    const size_t smem = smem_for(cs);
-    if (smem > kGemvSmemMax) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(gemv_w4a16_kernel<NB>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+template <int NB, int NW>
+cudaError_t launch_gemv_nb(const CUtensorMap& mapW, const GemvParams& p, int grid,
+                           cudaStream_t st) {
+    constexpr size_t smem = DecCfg<NW>::kSmem;
+    cudaError_t e = smem_attr_once<gemv_w4a16_kernel<NB, NW>>((int)smem);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(n_rb * cs));
-    cfg.blockDim = dim3(kGemvWarps * 32);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_w4a16_kernel<NB>, p, cs);
+    gemv_w4a16_kernel<NB, NW><<<grid, DecCfg<NW>::kThreads, smem, st>>>(mapW, p);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemv(const GemvParams& p, int num_sms, cudaStream_t st) {
+cudaError_t launch_gemv(const CUtensorMap& mapW, const GemvParams& p, int num_sms,
+                        cudaStream_t st) {
     if (p.M <= 0 || p.N <= 0) return cudaSuccess;
-    return p.M <= 8 ? launch_gemv_nb<1>(p, num_sms, st) : launch_gemv_nb<2>(p, num_sms, st);
+    const int64_t n_slabs = (p.N + kDecRows - 1) / kDecRows;
+    const int grid = (int)(n_slabs < num_sms ? n_slabs : num_sms);
+    // the kernel indexes a CTA's (slab, chunk) units in 32 bits
+    const int64_t cg = (p.G + kDecChunk - 1) / kDecChunk;
+    if ((n_slabs / grid + 1) * cg * 16 >= (1LL << 31)) return cudaErrorInvalidValue;
+    return p.M <= 8 ? launch_gemv_nb<1, 16>(mapW, p, grid, st)
+                    : launch_gemv_nb<2, 8>(mapW, p, grid, st);
 }
 
 }  // namespace awq

@@ -46,8 +46,11 @@ struct GemvParams {
     int G;
     uint16_t* Y;
     int64_t ldy;
+    unsigned* status;
 };
-cudaError_t launch_gemv(const GemvParams& p, int num_sms, cudaStream_t st);
+// mapW: 2-D tensor map of qweight as uint32 [N rows][K/8 words], box 80 words x 16 rows.
+cudaError_t launch_gemv(const CUtensorMap& mapW, const GemvParams& p, int num_sms,
+                        cudaStream_t st);
 
 // ---- tensor-core kernels (tc.cu): W4A16 GEMM and the alpha search ----
 struct TcParams {

@@ -321,13 +321,37 @@ __device__ void role_prod_gemm(const TcParams& p, uint8_t* As, SmemCtl* ctl, int
 }
 
 // ---- role: search producer (fake-quantise W diag(s), residual E in fp16) ----
-// Warp pw handles rows pw, pw + 16, ..., of the 128-row tile; each lane holds
-// 4 consecutive channels of the group.  The quantiser is the packer's, with
-// the same single-rounding fp32 steps.
+// Eight lanes hold one row of the group: lane c the channels 8c..8c+7 and
+// 64+8c..64+8c+7 (one 16-byte chunk in each 64-channel sub-tile, so the
+// eight lanes of a row fill 128 contiguous swizzled bytes per store).  A
+// warp covers 4 rows per pass, 16 warps x 2 passes the 128-row tile.  The
+// levels are the packer's (same rounding points), computed with the fast
+// exact quotient; E = (q - z) scale / s - W is formed as
+// ((q - z) scale - w') (1/s) in fp32 and rounded once to fp16.
+__device__ __forceinline__ void unpack8(uint4 v, float4 sa, float4 sb, float* wp) {
+    const __half2* h = reinterpret_cast<const __half2*>(&v);
+    const float2 f0 = __half22float2(h[0]), f1 = __half22float2(h[1]);
+    const float2 f2 = __half22float2(h[2]), f3 = __half22float2(h[3]);
+    wp[0] = __fmul_rn(f0.x, sa.x);
+    wp[1] = __fmul_rn(f0.y, sa.y);
+    wp[2] = __fmul_rn(f1.x, sa.z);
+    wp[3] = __fmul_rn(f1.y, sa.w);
+    wp[4] = __fmul_rn(f2.x, sb.x);
+    wp[5] = __fmul_rn(f2.y, sb.y);
+    wp[6] = __fmul_rn(f3.x, sb.z);
+    wp[7] = __fmul_rn(f3.y, sb.w);
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 template <int PW>
 __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, int pw, int lane) {
-    constexpr int kRowsPerWarp = kTcRows / PW;
+    static_assert(PW * 4 * 2 == kTcRows, "16 producer warps x 4 rows x 2 passes");
     volatile int* abort = &ctl->abort;
+    const int rr = lane >> 3, c = lane & 7;
     uint32_t a_iter = 0;
     bool bad = false;
     for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
@@ -335,50 +359,67 @@ __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, i
         const float* s_a = p.s_alpha + (int64_t)it.alpha * p.K;
         const float* is_a = p.inv_s_alpha + (int64_t)it.alpha * p.K;
         for (int g = 0; g < p.G; ++g) {
-            const int64_t k0 = (int64_t)g * kGroup + 4 * lane;
-            const float4 sv = __ldg(reinterpret_cast<const float4*>(s_a + k0));
-            const float4 iv = __ldg(reinterpret_cast<const float4*>(is_a + k0));
-            uint2 raw[kRowsPerWarp];
+            const int64_t k0 = (int64_t)g * kGroup + 8 * c;
+            uint4 raw[2][2];
 #pragma unroll
-            for (int i = 0; i < kRowsPerWarp; ++i) {
-                const int64_t n = (int64_t)it.n_tile * kTcRows + pw + PW * i;
-                raw[i] = n < p.N ? __ldg(reinterpret_cast<const uint2*>(p.W + n * p.ldw + k0))
-                                 : make_uint2(0, 0);
+            for (int ps = 0; ps < 2; ++ps) {
+                const int64_t n = (int64_t)it.n_tile * kTcRows + ps * 64 + pw * 4 + rr;
+                if (n < p.N) {
+                    const uint16_t* wr = p.W + n * p.ldw + k0;
+                    raw[ps][0] = __ldg(reinterpret_cast<const uint4*>(wr));
+                    raw[ps][1] = __ldg(reinterpret_cast<const uint4*>(wr + 64));
+                } else {
+                    raw[ps][0] = raw[ps][1] = make_uint4(0, 0, 0, 0);
+                }
             }
+            const float4 sv0 = __ldg(reinterpret_cast<const float4*>(s_a + k0));
+            const float4 sv1 = __ldg(reinterpret_cast<const float4*>(s_a + k0 + 4));
+            const float4 sv2 = __ldg(reinterpret_cast<const float4*>(s_a + k0 + 64));
+            const float4 sv3 = __ldg(reinterpret_cast<const float4*>(s_a + k0 + 68));
             const int st = a_iter % kNA;
             if (!mbar_wait(&ctl->a_empty[st], ((a_iter / kNA) & 1u) ^ 1u, abort, p.status)) return;
             uint8_t* tile = As + st * kAStage;
 #pragma unroll
-            for (int i = 0; i < kRowsPerWarp; ++i) {
-                const int r = pw + PW * i;
-                float w[4];
-                w[0] = __half2float(__ushort_as_half((unsigned short)(raw[i].x & 0xFFFFu)));
-                w[1] = __half2float(__ushort_as_half((unsigned short)(raw[i].x >> 16)));
-                w[2] = __half2float(__ushort_as_half((unsigned short)(raw[i].y & 0xFFFFu)));
-                w[3] = __half2float(__ushort_as_half((unsigned short)(raw[i].y >> 16)));
-                float wp[4];
-                wp[0] = __fmul_rn(w[0], sv.x);
-                wp[1] = __fmul_rn(w[1], sv.y);
-                wp[2] = __fmul_rn(w[2], sv.z);
-                wp[3] = __fmul_rn(w[3], sv.w);
-                float lo = fminf(fminf(wp[0], wp[1]), fminf(wp[2], wp[3]));
-                float hi = fmaxf(fmaxf(wp[0], wp[1]), fmaxf(wp[2], wp[3]));
-                bad |= !(isfinite(wp[0]) && isfinite(wp[1]) && isfinite(wp[2]) && isfinite(wp[3]));
-                const GroupQuant gq = group_quant_params(lo, hi);
-                bad |= !gq.finite;
-                const float is[4] = {iv.x, iv.y, iv.z, iv.w};
-                __half e[4];
+            for (int ps = 0; ps < 2; ++ps) {
+                const int r = ps * 64 + pw * 4 + rr;
+                float wp[16];
+                unpack8(raw[ps][0], sv0, sv1, wp);
+                unpack8(raw[ps][1], sv2, sv3, wp + 8);
+                float lo = wp[0], hi = wp[0];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float qf = quant_level(wp[j], gq);
-                    const float deq = __fmul_rn(__fsub_rn(qf, gq.zf), gq.scale);
-                    e[j] = __float2half_rn(__fmaf_rn(deq, is[j], -w[j]));
+                for (int e = 1; e < 16; ++e) {
+                    lo = fminf(lo, wp[e]);
+                    hi = fmaxf(hi, wp[e]);
                 }
-                uint2 o;
-                o.x = (uint32_t)__half_as_ushort(e[0]) | ((uint32_t)__half_as_ushort(e[1]) << 16);
-                o.y = (uint32_t)__half_as_ushort(e[2]) | ((uint32_t)__half_as_ushort(e[3]) << 16);
-                const int k = 4 * lane;
-                *reinterpret_cast<uint2*>(tile + (k >> 6) * kASub + sw128_offset(r, k & 63)) = o;
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) {
+                    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+                    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+                }
+                bad |= !(isfinite(lo) && isfinite(hi));
+                const GroupQuant gq = group_quant_from_range(lo, hi);
+                bad |= !gq.finite;
+                const float neg_z = -gq.zf, top_z = 15.0f - gq.zf;
+                uint32_t o[8];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float4 i0 = __ldg(reinterpret_cast<const float4*>(is_a + k0 + 64 * h));
+                    const float4 i1 = __ldg(reinterpret_cast<const float4*>(is_a + k0 + 64 * h + 4));
+                    const float is[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
+                    float e[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float w = wp[8 * h + j];
+                        const float qz = quant_level_mz(w, gq.scale, gq.rcp, neg_z, top_z);
+                        e[j] = __fmul_rn(__fsub_rn(__fmul_rn(qz, gq.scale), w), is[j]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) o[4 * h + j] = pack_h2(e[2 * j], e[2 * j + 1]);
+                }
+                *reinterpret_cast<uint4*>(tile + sw128_offset(r, 8 * c)) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4*>(tile + kASub + sw128_offset(r, 8 * c)) =
+                    make_uint4(o[4], o[5], o[6], o[7]);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -434,7 +475,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
         role_epilogue<MODE>(p, ctl, tmem, warp - kWarpEpi0, lane);
     } else if (warp >= kWarpProd0) {
-        if (MODE == kModeGemm)
+        if constexpr (MODE == kModeGemm)
             role_prod_gemm(p, As, ctl, (warp - kWarpProd0) * 32 + lane, lane);
         else
             role_prod_search<Cfg<MODE>::kProdWarps>(p, As, ctl, warp - kWarpProd0, lane);
@@ -451,9 +492,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
 template <int MODE>
 cudaError_t launch_tc(const CUtensorMap& mapX, const TcParams& p, int num_sms, cudaStream_t st) {
     if (p.n_items <= 0) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(tc_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    cudaError_t e = smem_attr_once<tc_kernel<MODE>>((int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = p.n_items < num_sms ? p.n_items : num_sms;
     tc_kernel<MODE><<<grid, Cfg<MODE>::kThreads, kSmemBytes, st>>>(mapX, p);
