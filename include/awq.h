@@ -183,6 +183,20 @@ awq_status w4a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
                       size_t ws_bytes, awq_stream_t stream);
 size_t w4a16_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
+/* Overlap of back-to-back decode matmuls (M <= 16).  Every decode launch
+ * lets the next kernel in the stream start beside it (programmatic dependent
+ * launch) and reads X / writes Y only after the previous kernel in the stream
+ * has completed.  With enable = 1 it also starts fetching its packed weights
+ * (qweight, scales, zeros) before that point, so consecutive matmuls keep
+ * HBM busy across kernel boundaries, as in a decode step where the weights
+ * are constant.  Enable it only if no kernel that writes a matmul's packed
+ * weights (awq_pack_int4 or any other) is the kernel immediately before that
+ * w4a16_gemm call in its stream; otherwise the matmul may read stale weights.
+ * Process-wide setting, default 0.  Returns AWQ_ERR_INVALID_ARG unless
+ * enable is 0 or 1.  (Host-side setting; the pages describe no counterpart
+ * beyond memory-bound decoding with fused 4-bit kernels.) */
+awq_status awq_set_weight_prefetch(int enable);
+
 /* ---- status and diagnostics ---------------------------------------------- */
 
 /* Synchronise `stream`, then return (and clear) the device-side status word

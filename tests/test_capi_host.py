@@ -76,6 +76,9 @@ def test_host_argument_checks(capi):
                                  None, base, None, None, 0, None) == 5
     # stats: bad accumulate flag
     assert capi.awq_act_stats(base, 4, 128, 128, 2, base, None) == 1
+    # decode weight prefetch: a flag, 0 or 1 only (host-side setting)
+    assert capi.awq_set_weight_prefetch(2) == 1
+    assert capi.awq_set_weight_prefetch(1) == 0 and capi.awq_set_weight_prefetch(0) == 0
     assert capi.awq_last_error_string()
 
 

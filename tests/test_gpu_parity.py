@@ -321,3 +321,28 @@ def test_decode_long_k_sampled(wb, orc, M):
     ns = np.tile(cols, M)
     ref = orc.w4a16_pairs(Xm, u32(qw), u16(sc), u16(ze), ms, ns)
     assert rel_err(y[ms, ns].astype(np.float64), ref) <= GEMM_TOL
+
+
+def test_decode_chain_early_weights(wb, orc):
+    """Back-to-back decode matmuls with early weight fetches enabled
+    (awq_set_weight_prefetch): each launch may start streaming its weights
+    while the previous one runs, as in a decode step where weights were
+    written long before.  Every output must still match the oracle."""
+    layers = []
+    for j, (N, K, M) in enumerate([(1024, 1024, 1), (520, 2304, 3), (2048, 4096, 1),
+                                   (4096, 11008, 8), (136, 384, 16)]):
+        W, _, X, _ = sg.layer_inputs(30, j, N, K, 0, M=M)
+        rq, rs, rz = orc.pack_int4(W)
+        ref = orc.w4a16_gemm(X, rq, rs, rz)
+        layers.append((dev(X), dev(rq.view(np.int32)), dev(rs.view(np.float16)),
+                       dev(rz.view(np.float16)), ref))
+    torch.cuda.synchronize()
+    wb.set_weight_prefetch(True)
+    try:
+        for _ in range(3):
+            outs = [wb.w4a16_gemm(x, q, s, z) for (x, q, s, z, _) in layers]
+            for y, layer in zip(outs, layers):
+                assert rel_err(host(y), layer[4]) <= GEMM_TOL
+        wb.sync_status()
+    finally:
+        wb.set_weight_prefetch(False)

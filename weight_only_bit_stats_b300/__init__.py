@@ -21,7 +21,8 @@ import os
 import torch
 
 __all__ = ["AwqError", "lib", "act_stats", "act_mean", "candidate_scales", "search_scale",
-           "pack_int4", "w4a16_gemm", "sync_status", "ALPHA_GRID", "GROUP"]
+           "pack_int4", "w4a16_gemm", "set_weight_prefetch", "sync_status", "ALPHA_GRID",
+           "GROUP"]
 
 GROUP = 128
 ALPHA_GRID = tuple(i / 20.0 for i in range(20))
@@ -58,6 +59,7 @@ SIGNATURES = (
     ("awq_pack_int4", _int, [_p, _i64, _i64, _i64, _p, _int, _p, _p, _p, _p]),
     ("w4a16_gemm", _int, [_p, _i64, _i64, _i64, _p, _p, _p, _i64, _int, _p, _i64, _p, _sz, _p]),
     ("w4a16_gemm_workspace_size", _sz, [_i64, _i64, _i64]),
+    ("awq_set_weight_prefetch", _int, [_int]),
     ("awq_sync_status", _int, [_p]),
     ("awq_last_error_string", ctypes.c_char_p, []),
     ("awq_version", _int, []),
@@ -223,6 +225,14 @@ def w4a16_gemm(X: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, zer
                             ws.data_ptr() if ws is not None else None, ws_n, _stream(stream)),
            "w4a16_gemm")
     return Y
+
+
+def set_weight_prefetch(enable: bool) -> None:
+    """Allow decode matmuls to fetch their packed weights before the previous
+    kernel in the stream completes (see ``awq_set_weight_prefetch``); only
+    valid when no kernel writing a matmul's weights runs immediately before
+    it in the same stream."""
+    _check(lib().awq_set_weight_prefetch(1 if enable else 0), "awq_set_weight_prefetch")
 
 
 def sync_status(stream=None) -> None:

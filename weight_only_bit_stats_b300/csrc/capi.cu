@@ -4,6 +4,7 @@
 // caller's workspace.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "awq.h"
@@ -11,6 +12,9 @@
 #include "kernels.cuh"
 
 namespace {
+
+// awq_set_weight_prefetch() state, read by every decode launch.
+std::atomic<int> g_early_weights{0};
 
 // Device status word (one per device that loads the library).
 __device__ unsigned int g_awq_status;
@@ -96,13 +100,13 @@ awq_status make_act_map(CUtensorMap* map, const uint16_t* X, int64_t rows, int64
 }
 
 // Packed weights [N, K/8] uint32 for the decode kernel: unswizzled boxes of
-// 80 words (five groups of 128 nibbles) x 16 rows, landing as
-// [16 rows][320 B].
+// 48 words (three groups of 128 nibbles) x 16 rows, landing as
+// [16 rows][192 B].
 awq_status make_qweight_map(CUtensorMap* map, const uint32_t* qw, int64_t N, int64_t K) {
     if (!load_encoder()) return fail(AWQ_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
     cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)N};
     cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-    cuuint32_t box[2] = {80, 16};
+    cuuint32_t box[2] = {48, 16};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(qw), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -144,6 +148,12 @@ awq_status report_error(awq_status code, const char* msg) { return fail(code, ms
 extern "C" {
 
 int awq_version(void) { return 100; }
+
+awq_status awq_set_weight_prefetch(int enable) {
+    if (enable != 0 && enable != 1) return fail(AWQ_ERR_INVALID_ARG, "set_weight_prefetch: flag must be 0 or 1");
+    g_early_weights.store(enable, std::memory_order_relaxed);
+    return AWQ_OK;
+}
 
 const char* awq_last_error_string(void) { return g_last_error; }
 
@@ -343,7 +353,7 @@ awq_status w4a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx, cons
         s = make_qweight_map(&map, qweight, N, K);
         if (s) return s;
         awq::GemvParams p = {X, ldx, (int)M, qweight, scales, zeros, N, K, (int)(K / AWQ_GROUP),
-                             Y, ldy, d->status};
+                             Y, ldy, d->status, g_early_weights.load(std::memory_order_relaxed)};
         e = awq::launch_gemv(map, p, d->num_sms, st);
     } else {
         CUtensorMap map;

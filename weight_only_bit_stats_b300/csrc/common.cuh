@@ -65,20 +65,48 @@ __device__ __forceinline__ float rint_small(float x) {
     return __fsub_rn(__fadd_rn(x, c), c);
 }
 
-// rint(fp32(a / b)) exactly, given rb = fp32(1 / b) correctly rounded.
-// t0 = fp32(a * rb) carries two rounding errors of at most 2^-24 relative
-// each, so |t0 - fp32(a / b)| <= 3 * 2^-24 |t0| (to first order).  When no
-// half-integer lies within 2^-21 |t0| of t0 -- margin 2.6x that bound, and
-// the margin itself is computed exactly for |t0| >= 1/4 (Sterbenz), while
-// below 1/4 both roundings give 0 -- rint(t0) is rint(fp32(a / b)).
-// Otherwise (near a tie, |t0| >= 2^22, Inf, NaN) the quotient is formed by
-// IEEE division.  The fast path uses no XU instruction.
+// rint(fp32(a / b)) wherever it can change a level, given rb = fp32(1 / b)
+// correctly rounded.  Every caller clamps the result (plus a zero-point in
+// 0..15) to 0..15, so only |a / b| < 32 needs the exact integer; beyond that
+// any value of the same sign and at least 16 in magnitude clamps alike.
+// t0 = fp32(a * rb) carries two roundings of at most 2^-24 relative each,
+// so |t0 - fp32(a / b)| <= 3 * 2^-24 |t0| < 2^-16 for |t0| < 32.  Hence
+// when t0 is more than 2^-16 away from the nearest half-integer (the test
+// below), fp32(a / b) rounds to the same integer as t0.  Near a tie the
+// quotient is formed by IEEE division.  For |t0| >= 32 the fast value keeps
+// the sign and stays >= 16 in magnitude (rint_small errs by at most 2 past
+// 2^22), so the clamped level is the same; Inf and NaN reach the same clamp
+// on both paths.  The fast path uses no XU instruction.
+constexpr float kTieBand = 0.4999847412109375f;   // 0.5 - 2^-16
+
+__device__ __forceinline__ bool near_tie(float t0, float rt) {
+    return fabsf(__fsub_rn(t0, rt)) > kTieBand;
+}
+
 __device__ __forceinline__ float rint_quot(float a, float b, float rb) {
     const float t0 = __fmul_rn(a, rb);
     const float rt = rint_small(t0);
-    const float margin = __fsub_rn(0.5f, fabsf(__fsub_rn(t0, rt)));
-    if (margin > __fmul_rn(fabsf(t0), 4.76837158203125e-07f)) return rt;   // 2^-21
-    return rintf(__fdiv_rn(a, b));
+    if (near_tie(t0, rt)) return rintf(__fdiv_rn(a, b));
+    return rt;
+}
+
+// rint_quot for 8 values of one warp-uniform divisor, without a branch per
+// value: the fast roundings first, then -- only if some lane of the warp
+// met a near-tie -- the exact quotient for those values.  All 32 lanes of
+// the warp must call it together.
+__device__ __forceinline__ void rint_quot8(const float* a, float b, float rb, float* r) {
+    bool tie = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float t0 = __fmul_rn(a[j], rb);
+        r[j] = rint_small(t0);
+        tie |= near_tie(t0, r[j]);
+    }
+    if (__any_sync(0xffffffffu, tie)) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (near_tie(__fmul_rn(a[j], rb), r[j])) r[j] = rintf(__fdiv_rn(a[j], b));
+    }
 }
 
 struct GroupQuant {

@@ -7,17 +7,15 @@
 //
 //  * Persistent grid, one CTA per SM.  CTA c owns a balanced, contiguous run
 //    of 16-row slabs; its consumer warps (16 for up to 8 tokens, else 8)
-//    split the CTA's (slab, 5-group chunk) units into equal contiguous
+//    split the CTA's (slab, 3-group chunk) units into equal contiguous
 //    ranges, so a slab can be shared by neighbouring warps (intra-CTA
 //    split-K).
 //  * Each warp streams its units through its own ring in shared memory,
-//    filled by TMA: one 2-D box of 16 rows x 5 groups (320 contiguous bytes
-//    per row) per unit.  With a 320-byte row pitch the fragment reads of a
-//    quarter warp (two rows, 4 x 16 B each) fall on disjoint bank halves.
-//    Narrow boxes (one 64-byte group per row) are not used: on B300 the TMA
-//    then issues one small request per row and delivers only about 1 TB/s.
-//    Every warp's whole ring is requested at kernel start: 160 KB per SM in
-//    flight.
+//    filled by TMA: one 2-D box of 16 rows x 3 groups (192 contiguous bytes
+//    per row) per unit.  With a 192-byte row pitch (an odd multiple of 64)
+//    the fragment reads of a quarter warp (two rows, 4 x 16 B each) fall on
+//    disjoint bank halves.  Every warp's whole ring is requested at kernel
+//    start: 96 KB per SM in flight (16 warps x 2 stages x 3 KB).
 //  * Nibbles become exact fp16 values (q - z) in registers: a LOP3 places a
 //    nibble in the mantissa of 1024.0 (or 1024 + 16 q for the high nibble of
 //    a byte), and one HSUB2 / HFMA2 removes the offset and the zero-point.
@@ -26,9 +24,14 @@
 //    mma.m16n8k16 (fp16 in, fp32 accumulate), which keeps the M FMAs per
 //    weight off the FP32 pipe.  The MMA's k order is a permutation of the
 //    physical k order chosen so that each thread's 16 loaded bytes of a row
-//    are exactly its A fragment; each thread reads the matching 64 bytes of
-//    activations (L1-resident) and applies the same permutation with PRMT.
-//    The group scale is applied in fp32 to the per-group partial sums.
+//    are exactly its A fragment; the activations are staged once per CTA in
+//    shared memory under the same permutation (or, when they do not fit,
+//    read through L1 and permuted with PRMT).  The group scale is applied in
+//    fp32 to the per-group partial sums.
+//  * Programmatic dependent launch: the next kernel in the stream is released
+//    at once and may take an SM as soon as this kernel's CTA there retires;
+//    when the caller allows early weight reads it streams its first weights
+//    before waiting for this kernel to complete.
 //  * A slab owned by one warp is written straight from registers; a slab
 //    shared by several warps is reduced through shared memory in warp order.
 //    The work split depends on N and K only, so the result is deterministic
@@ -44,25 +47,37 @@ constexpr int kDecRows = 16;                        // rows per slab (MMA M)
 // (row pitch kDecChunk * 64 B in shared memory).  An odd count makes the
 // pitch an odd multiple of 64 B, so the two rows a quarter warp reads sit on
 // disjoint bank halves; wide rows keep the TMA's per-row request count low.
-constexpr int kDecChunk = 5;
-constexpr int kDecPitch = kDecChunk * 64;                     // 320 B
-constexpr int kDecStageBytes = kDecRows * kDecPitch;          // 5 KB
+constexpr int kDecChunk = 3;
+constexpr int kDecPitch = kDecChunk * 64;                     // 192 B
+constexpr int kDecStageBytes = kDecRows * kDecPitch;          // 3 KB
 static_assert(kDecChunk % 2 == 1, "row pitch must be an odd multiple of 64 bytes");
 
-// Consumer warps per CTA: 16 with a 2-stage ring each for up to 8 tokens,
-// 8 (more registers each) with a 3-stage ring for 9..16 tokens.
-template <int NW>
+// Per token-tile count NB (1: up to 8 tokens, 2: up to 16): 16 consumer
+// warps with a 2-stage ring each for NB = 1, 8 warps (more registers each)
+// with a 3-stage ring for NB = 2.  One CTA per SM.
+template <int NB>
 struct DecCfg {
-    static constexpr int kThreads = NW * 32;
-    static constexpr int kStages = NW >= 16 ? 2 : 3;
-    static constexpr int kSlots = 2 * NW;           // partial sums: first/last slab of each warp
-    static constexpr size_t kRingBytes = (size_t)NW * kStages * kDecStageBytes;
-    static constexpr size_t kPartBytes = (size_t)kSlots * kDecRows * 16 * sizeof(float);
-    static constexpr size_t kCtlBytes = (size_t)NW * kStages * 8 + (size_t)NW * 12 + 16;
+    static constexpr int kWarps = NB == 1 ? 16 : 8;
+    static constexpr int kThreads = kWarps * 32;
+    static constexpr int kMinBlocks = 1;
+    static constexpr int kStages = NB == 1 ? 2 : 3;
+    static constexpr int kCols = 8 * NB;                // token columns (8 per MMA n-tile)
+    static constexpr int kSlots = 2 * kWarps;           // partial sums: first/last slab of each warp
+    static constexpr size_t kRingBytes = (size_t)kWarps * kStages * kDecStageBytes;
+    static constexpr size_t kPartBytes = (size_t)kSlots * kDecRows * kCols * sizeof(float);
+    static constexpr size_t kCtlBytes = (size_t)kWarps * 3 * 8 + (size_t)kWarps * 12 + 16;
+    // fixed part; the staged activations (when they fit) follow it
     static constexpr size_t kSmem = 1024 + kRingBytes + kPartBytes + kCtlBytes;
 };
-static_assert(DecCfg<16>::kSmem <= 232448 && DecCfg<8>::kSmem <= 232448,
+constexpr size_t kDecSmemMax = 232448;                 // per-block opt-in limit on sm_103
+static_assert(DecCfg<1>::kSmem <= kDecSmemMax && DecCfg<2>::kSmem <= kDecSmemMax,
               "decode kernel exceeds shared memory");
+
+// Shared-memory activations: per token a row of G * 256 + 64 bytes; within
+// a group, the 8-element chunk of physical k = 32 t + 8 i sits at chunk
+// position 4 i + t already in fragment order (x0,x4)(x1,x5)(x2,x6)(x3,x7).
+// The 64-byte pad puts consecutive tokens on different bank halves.
+__host__ __device__ constexpr int64_t dec_x_row_bytes(int64_t G) { return G * 256 + 64; }
 
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t d;
@@ -114,44 +129,61 @@ __device__ __forceinline__ uint4 permute_x8(uint4 v) {
     return o;
 }
 
-// Per-group operands a thread needs besides the weights: the scale and
-// zero-point of its two rows, and its 64 bytes of each token's activations.
+// Scale and zero-point of a thread's two rows for the groups of one chunk,
+// loaded one chunk ahead.
+struct ChunkSZ {
+    uint16_t sa[kDecChunk], sb[kDecChunk], za[kDecChunk], zb[kDecChunk];
+};
+
+__device__ __forceinline__ void load_chunk_sz(ChunkSZ& z, const GemvParams& p, int64_t row_a,
+                                              int gb) {
+    const bool va = row_a < p.N, vb = row_a + 8 < p.N;
+    const uint16_t* sa = p.scales + (va ? row_a : 0) * p.G;
+    const uint16_t* za = p.zeros + (va ? row_a : 0) * p.G;
+    const uint16_t* sb = p.scales + (vb ? row_a + 8 : 0) * p.G;
+    const uint16_t* zb = p.zeros + (vb ? row_a + 8 : 0) * p.G;
+#pragma unroll
+    for (int j = 0; j < kDecChunk; ++j) {
+        const int gi = gb + j;
+        const bool in = gi < p.G;
+        z.sa[j] = (va && in) ? __ldg(sa + gi) : (uint16_t)0;
+        z.za[j] = (va && in) ? __ldg(za + gi) : (uint16_t)0;
+        z.sb[j] = (vb && in) ? __ldg(sb + gi) : (uint16_t)0;
+        z.zb[j] = (vb && in) ? __ldg(zb + gi) : (uint16_t)0;
+    }
+}
+
+// A thread's 64 bytes of each token's activations for one group, in
+// fragment order (used when the activations are not staged in shared memory).
 template <int NB>
-struct GroupIn {
-    uint16_t sa, sb, za, zb;
+struct GroupX {
     uint4 x[NB][4];
 };
 
 template <int NB>
-__device__ __forceinline__ void load_group_in(GroupIn<NB>& in, const GemvParams& p, int64_t row_a,
-                                              int gi, int g, int t) {
-    const bool va = row_a < p.N, vb = row_a + 8 < p.N;
-    in.sa = va ? __ldg(p.scales + row_a * p.G + gi) : (uint16_t)0;
-    in.za = va ? __ldg(p.zeros + row_a * p.G + gi) : (uint16_t)0;
-    in.sb = vb ? __ldg(p.scales + (row_a + 8) * p.G + gi) : (uint16_t)0;
-    in.zb = vb ? __ldg(p.zeros + (row_a + 8) * p.G + gi) : (uint16_t)0;
+__device__ __forceinline__ void load_group_x(GroupX<NB>& in, const GemvParams& p, int gi, int g,
+                                             int t) {
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
-        const int tok = g + 8 * nb;
-        if (tok < p.M) {
-            const uint4* xp = reinterpret_cast<const uint4*>(p.X + (int64_t)tok * p.ldx +
-                                                             (int64_t)gi * kGroup + 32 * t);
+        // lanes of absent tokens read the last token (their column is dropped)
+        const int tok = min(g + 8 * nb, p.M - 1);
+        const uint4* xp = reinterpret_cast<const uint4*>(p.X + (int64_t)tok * p.ldx +
+                                                         (int64_t)gi * kGroup + 32 * t);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) in.x[nb][i] = __ldg(xp + i);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) in.x[nb][i] = make_uint4(0, 0, 0, 0);
-        }
+        for (int i = 0; i < 4; ++i) in.x[nb][i] = permute_x8(__ldg(xp + i));
     }
 }
 
 // y += scale * (X_group (q - z)^T) for one group: 8 (16 for NB = 2) MMAs in
-// four independent accumulator chains (one per packed word), added in a
-// fixed order.
-template <int NB>
-__device__ __forceinline__ void group_mma(float (&y)[NB][4], const GroupIn<NB>& in, uint4 wa,
-                                          uint4 wb) {
-    const __half za = __ushort_as_half(in.za), zb = __ushort_as_half(in.zb);
+// two independent accumulator chains, added in a fixed order.  xs: this
+// thread's staged activation rows (XS), one per n-tile, or null for a token
+// beyond M.
+template <int NB, bool XS>
+__device__ __forceinline__ void group_mma(float (&y)[NB][4], uint16_t sa16, uint16_t sb16,
+                                          uint16_t za16, uint16_t zb16, const GroupX<NB>& gx,
+                                          uint4 wa, uint4 wb, const uint8_t* const (&xs)[NB],
+                                          int gi, int t) {
+    const __half za = __ushort_as_half(za16), zb = __ushort_as_half(zb16);
     const __half h1024 = __float2half_rn(1024.0f), h64 = __float2half_rn(64.0f);
     const __half2 za1024 = __half2half2(__hadd(h1024, za));
     const __half2 zb1024 = __half2half2(__hadd(h1024, zb));
@@ -159,11 +191,11 @@ __device__ __forceinline__ void group_mma(float (&y)[NB][4], const GroupIn<NB>& 
     const __half2 zbneg = __half2half2(__hneg(__hadd(h64, zb)));
     const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
     const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
-    float c[NB][4][4];
+    float c[NB][2][4];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) c[nb][i][j] = 0.0f;
 #pragma unroll
@@ -173,28 +205,29 @@ __device__ __forceinline__ void group_mma(float (&y)[NB][4], const GroupIn<NB>& 
         dequant_word(wB[i], zb1024, zbneg, pb);
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
-            const uint4 b = permute_x8(in.x[nb][i]);
-            mma16816(c[nb][i], pa[0], pb[0], pa[1], pb[1], b.x, b.y);
-            mma16816(c[nb][i], pa[2], pb[2], pa[3], pb[3], b.z, b.w);
+            uint4 b;
+            if constexpr (XS) {
+                b = *reinterpret_cast<const uint4*>(xs[nb] + gi * 256 + (i * 4 + t) * 16);
+            } else {
+                b = gx.x[nb][i];
+            }
+            mma16816(c[nb][i & 1], pa[0], pb[0], pa[1], pb[1], b.x, b.y);
+            mma16816(c[nb][i & 1], pa[2], pb[2], pa[3], pb[3], b.z, b.w);
         }
     }
-    const float fsa = __half2float(__ushort_as_half(in.sa));
-    const float fsb = __half2float(__ushort_as_half(in.sb));
+    const float fsa = __half2float(__ushort_as_half(sa16));
+    const float fsb = __half2float(__ushort_as_half(sb16));
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
-        float s[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            s[j] = (c[nb][0][j] + c[nb][1][j]) + (c[nb][2][j] + c[nb][3][j]);
-        y[nb][0] = fmaf(fsa, s[0], y[nb][0]);
-        y[nb][1] = fmaf(fsa, s[1], y[nb][1]);
-        y[nb][2] = fmaf(fsb, s[2], y[nb][2]);
-        y[nb][3] = fmaf(fsb, s[3], y[nb][3]);
+        y[nb][0] = fmaf(fsa, c[nb][0][0] + c[nb][1][0], y[nb][0]);
+        y[nb][1] = fmaf(fsa, c[nb][0][1] + c[nb][1][1], y[nb][1]);
+        y[nb][2] = fmaf(fsb, c[nb][0][2] + c[nb][1][2], y[nb][2]);
+        y[nb][3] = fmaf(fsb, c[nb][0][3] + c[nb][1][3], y[nb][3]);
     }
 }
 
-// First unit of warp j when U units are split over NW warps (NW a power of
-// two, so the division is a shift).
+// First unit of warp j when U units are split over NW warps (division by a
+// compile-time constant).
 template <int NW>
 __device__ __forceinline__ int warp_lo(int U, int j) {
     return (int)(((int64_t)j * U) / NW);
@@ -202,18 +235,20 @@ __device__ __forceinline__ int warp_lo(int U, int j) {
 
 template <int NW>
 struct DecCtl {
-    uint64_t full[NW][DecCfg<NW>::kStages];
+    uint64_t full[NW][3];
     int w_lo[NW], w_hi[NW], w_first[NW];    // each warp's unit range and first slab
     int abort;
 };
-static_assert(sizeof(DecCtl<16>) <= DecCfg<16>::kCtlBytes &&
-                  sizeof(DecCtl<8>) <= DecCfg<8>::kCtlBytes,
+static_assert(sizeof(DecCtl<16>) <= DecCfg<1>::kCtlBytes &&
+                  sizeof(DecCtl<8>) <= DecCfg<2>::kCtlBytes && DecCfg<1>::kStages <= 3 &&
+                  DecCfg<2>::kStages <= 3,
               "control block does not fit its shared-memory slot");
 
-template <int NB, int NW>
-__global__ void __launch_bounds__(NW * 32, 1)
+template <int NB, int NW, bool XS>
+__global__ void __launch_bounds__(NW * 32, DecCfg<NB>::kMinBlocks)
     gemv_w4a16_kernel(const __grid_constant__ CUtensorMap mapW, const GemvParams p) {
-    using Cfg = DecCfg<NW>;
+    using Cfg = DecCfg<NB>;
+    static_assert(Cfg::kWarps == NW, "warp count");
     constexpr int kDecWarps = NW;
     constexpr int kDecThreads = Cfg::kThreads;
     constexpr int kDecStages = Cfg::kStages;
@@ -223,6 +258,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     uint8_t* ring = smem;
     float* part = reinterpret_cast<float*>(smem + Cfg::kRingBytes);
     DecCtl<NW>* ctl = reinterpret_cast<DecCtl<NW>*>(smem + Cfg::kRingBytes + Cfg::kPartBytes);
+    uint8_t* xsm = smem + Cfg::kRingBytes + Cfg::kPartBytes + Cfg::kCtlBytes;   // XS only
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
 
@@ -263,9 +299,43 @@ __global__ void __launch_bounds__(NW * 32, 1)
         tma_load_2d(my_ring + (size_t)s * kDecStageBytes, &mapW, bar, ch * kDecChunk * 16,
                     (s0 + sl) * kDecRows);
     };
-    if (lane == 0)
+    // Programmatic dependent launch: the next kernel in the stream may be
+    // scheduled beside this one right away.  This kernel reads X and writes Y
+    // only after griddepcontrol.wait, i.e. after the previous kernel has
+    // completed and flushed; with early_weights (the caller's guarantee that
+    // the previous kernel does not write the packed weights) the first ring
+    // stages of weights are requested before that wait.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (p.early_weights && lane == 0)
+        for (int i = 0; i < kDecStages && i < n_my; ++i) issue(u_lo + i, i);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!p.early_weights && lane == 0)
         for (int i = 0; i < kDecStages && i < n_my; ++i) issue(u_lo + i, i);
     __syncwarp();
+
+    // stage the activations in fragment order while the first weights stream in
+    const uint8_t* xs[NB];
+    if constexpr (XS) {
+        const int64_t xrow = dec_x_row_bytes(p.G);
+        const int chunks = p.M * p.G * 16;
+        for (int cix = threadIdx.x; cix < chunks; cix += kDecThreads) {
+            const int m = cix / (p.G * 16), rem = cix - m * p.G * 16;
+            const int gl = rem >> 4, k8 = rem & 15;
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+                p.X + (int64_t)m * p.ldx + (int64_t)gl * kGroup + k8 * 8));
+            const int tt = k8 >> 2, ii = k8 & 3;
+            *reinterpret_cast<uint4*>(xsm + m * xrow + gl * 256 + (ii * 4 + tt) * 16) =
+                permute_x8(v);
+        }
+        __syncthreads();
+        // an MMA output column depends only on its own B column, so lanes of
+        // absent tokens read the last token's row and their outputs are dropped
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) xs[nb] = xsm + min(g + 8 * nb, p.M - 1) * xrow;
+    } else {
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) xs[nb] = nullptr;
+    }
 
     // write a finished slab: straight to Y when this warp owns the whole
     // slab, else into this warp's first/last partial slot
@@ -285,14 +355,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 }
         } else {
             const int slot = 2 * warp + (sl == first_sl ? 0 : 1);
-            float* dst = part + (size_t)slot * kDecRows * 16;
+            float* dst = part + (size_t)slot * kDecRows * Cfg::kCols;
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int tok = nb * 8 + 2 * t + (j & 1);
                     const int rl = g + ((j < 2) ? 0 : 8);
-                    dst[rl * 16 + tok] = y[nb][j];
+                    dst[rl * Cfg::kCols + tok] = y[nb][j];
                 }
         }
     };
@@ -304,6 +374,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
         for (int j = 0; j < 4; ++j) y[nb][j] = 0.0f;
     int cur = -1;
     int sl = first_sl, ch = u_lo - first_sl * CG;       // (slab, chunk) of unit u_lo + i
+    ChunkSZ sz;
+    if (n_my > 0) load_chunk_sz(sz, p, (int64_t)(s0 + sl) * kDecRows + g, ch * kDecChunk);
     int i = 0;
     bool ok = true;
     for (; i < n_my; ++i) {
@@ -315,11 +387,17 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 for (int j = 0; j < 4; ++j) y[nb][j] = 0.0f;
             cur = sl;
         }
-        const int64_t row_a = (int64_t)(s0 + sl) * kDecRows + g;
         const int gb = ch * kDecChunk, ge = min(p.G, gb + kDecChunk);
-        // operands of the chunk's first group go out before the wait
-        GroupIn<NB> nxt;
-        load_group_in<NB>(nxt, p, row_a, gb, g, t);
+        // the next unit's scales and zero-points go out a chunk ahead
+        int nsl = sl, nch = ch + 1;
+        if (nch == CG) {
+            nch = 0;
+            ++nsl;
+        }
+        ChunkSZ nsz;
+        if (i + 1 < n_my) load_chunk_sz(nsz, p, (int64_t)(s0 + nsl) * kDecRows + g, nch * kDecChunk);
+        GroupX<NB> gx;
+        if constexpr (!XS) load_group_x<NB>(gx, p, gb, g, t);
         const int s = i % kDecStages;
         if (!mbar_wait(&ctl->full[warp][s], (uint32_t)(i / kDecStages) & 1u, &ctl->abort,
                        p.status)) {
@@ -331,12 +409,16 @@ __global__ void __launch_bounds__(NW * 32, 1)
         for (int jg = 0; jg < kDecChunk; ++jg) {
             const int gi = gb + jg;
             if (gi < ge) {
-                const GroupIn<NB> in = nxt;
-                if (gi + 1 < ge) load_group_in<NB>(nxt, p, row_a, gi + 1, g, t);
+                GroupX<NB> cx;
+                if constexpr (!XS) {
+                    cx = gx;
+                    if (gi + 1 < ge) load_group_x<NB>(gx, p, gi + 1, g, t);
+                }
                 const uint8_t* gbox = box + jg * 64 + t * 16;
                 const uint4 wa = *reinterpret_cast<const uint4*>(gbox + g * kDecPitch);
                 const uint4 wb = *reinterpret_cast<const uint4*>(gbox + (g + 8) * kDecPitch);
-                group_mma<NB>(y, in, wa, wb);
+                group_mma<NB, XS>(y, sz.sa[jg], sz.sb[jg], sz.za[jg], sz.zb[jg], cx, wa, wb, xs,
+                                  gi, t);
             }
         }
         __syncwarp();
@@ -345,10 +427,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
             fence_proxy_async_smem();
             issue(u_lo + i + kDecStages, s);
         }
-        if (++ch == CG) {
-            ch = 0;
-            ++sl;
-        }
+        sz = nsz;
+        sl = nsl;
+        ch = nch;
     }
     if (ok && cur >= 0) flush(cur, y);
     if (!ok && lane == 0) {
@@ -376,7 +457,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
                     const int lo = ctl->w_lo[j], hi = ctl->w_hi[j];
                     if (hi <= lo || hi <= rsl * CG || lo >= (rsl + 1) * CG) continue;
                     const int slot = 2 * j + (ctl->w_first[j] == rsl ? 0 : 1);
-                    acc += part[(slot * kDecRows + r) * 16 + m];
+                    acc += part[(slot * kDecRows + r) * Cfg::kCols + m];
                 }
                 const int64_t row = row0 + r;
                 if (row < p.N)
@@ -386,14 +467,32 @@ __global__ void __launch_bounds__(NW * 32, 1)
     }
 }
 
-template <int NB, int NW>
-cudaError_t launch_gemv_nb(const CUtensorMap& mapW, const GemvParams& p, int grid,
+template <int NB, int NW, bool XS>
+cudaError_t launch_gemv_nb(const CUtensorMap& mapW, const GemvParams& p, int grid, size_t smem,
                            cudaStream_t st) {
-    constexpr size_t smem = DecCfg<NW>::kSmem;
-    cudaError_t e = smem_attr_once<gemv_w4a16_kernel<NB, NW>>((int)smem);
+    cudaError_t e = smem_attr_once<gemv_w4a16_kernel<NB, NW, XS>>((int)kDecSmemMax);
     if (e != cudaSuccess) return e;
-    gemv_w4a16_kernel<NB, NW><<<grid, DecCfg<NW>::kThreads, smem, st>>>(mapW, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(DecCfg<NB>::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_w4a16_kernel<NB, NW, XS>, mapW, p);
+}
+
+template <int NB, int NW>
+cudaError_t launch_gemv_cfg(const CUtensorMap& mapW, const GemvParams& p, int grid,
+                            cudaStream_t st) {
+    // stage the activations in shared memory when they fit beside the ring
+    const size_t xs_bytes = (size_t)p.M * (size_t)dec_x_row_bytes(p.G);
+    if (DecCfg<NB>::kSmem + xs_bytes <= kDecSmemMax)
+        return launch_gemv_nb<NB, NW, true>(mapW, p, grid, DecCfg<NB>::kSmem + xs_bytes, st);
+    return launch_gemv_nb<NB, NW, false>(mapW, p, grid, DecCfg<NB>::kSmem, st);
 }
 
 }  // namespace
@@ -406,8 +505,8 @@ cudaError_t launch_gemv(const CUtensorMap& mapW, const GemvParams& p, int num_sm
     // the kernel indexes a CTA's (slab, chunk) units in 32 bits
     const int64_t cg = (p.G + kDecChunk - 1) / kDecChunk;
     if ((n_slabs / grid + 1) * cg * 16 >= (1LL << 31)) return cudaErrorInvalidValue;
-    return p.M <= 8 ? launch_gemv_nb<1, 16>(mapW, p, grid, st)
-                    : launch_gemv_nb<2, 8>(mapW, p, grid, st);
+    return p.M <= 8 ? launch_gemv_cfg<1, 16>(mapW, p, grid, st)
+                    : launch_gemv_cfg<2, 8>(mapW, p, grid, st);
 }
 
 }  // namespace awq

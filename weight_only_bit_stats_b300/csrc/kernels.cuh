@@ -47,8 +47,9 @@ struct GemvParams {
     uint16_t* Y;
     int64_t ldy;
     unsigned* status;
+    int early_weights;   // 1: weights may be fetched before the previous kernel completes
 };
-// mapW: 2-D tensor map of qweight as uint32 [N rows][K/8 words], box 80 words x 16 rows.
+// mapW: 2-D tensor map of qweight as uint32 [N rows][K/8 words], box 48 words x 16 rows.
 cudaError_t launch_gemv(const CUtensorMap& mapW, const GemvParams& p, int num_sms,
                         cudaStream_t st);
 

@@ -372,10 +372,6 @@ __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, i
                     raw[ps][0] = raw[ps][1] = make_uint4(0, 0, 0, 0);
                 }
             }
-            const float4 sv0 = __ldg(reinterpret_cast<const float4*>(s_a + k0));
-            const float4 sv1 = __ldg(reinterpret_cast<const float4*>(s_a + k0 + 4));
-            const float4 sv2 = __ldg(reinterpret_cast<const float4*>(s_a + k0 + 64));
-            const float4 sv3 = __ldg(reinterpret_cast<const float4*>(s_a + k0 + 68));
             const int st = a_iter % kNA;
             if (!mbar_wait(&ctl->a_empty[st], ((a_iter / kNA) & 1u) ^ 1u, abort, p.status)) return;
             uint8_t* tile = As + st * kAStage;
@@ -383,8 +379,11 @@ __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, i
             for (int ps = 0; ps < 2; ++ps) {
                 const int r = ps * 64 + pw * 4 + rr;
                 float wp[16];
-                unpack8(raw[ps][0], sv0, sv1, wp);
-                unpack8(raw[ps][1], sv2, sv3, wp + 8);
+                {   // s is the same for every row: L1-resident, reloaded per pass
+                    const float4* sp = reinterpret_cast<const float4*>(s_a + k0);
+                    unpack8(raw[ps][0], __ldg(sp), __ldg(sp + 1), wp);
+                    unpack8(raw[ps][1], __ldg(sp + 16), __ldg(sp + 17), wp + 8);
+                }
                 float lo = wp[0], hi = wp[0];
 #pragma unroll
                 for (int e = 1; e < 16; ++e) {
@@ -407,10 +406,11 @@ __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, i
                     const float4 i1 = __ldg(reinterpret_cast<const float4*>(is_a + k0 + 64 * h + 4));
                     const float is[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
                     float e[8];
+                    rint_quot8(wp + 8 * h, gq.scale, gq.rcp, e);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const float w = wp[8 * h + j];
-                        const float qz = quant_level_mz(w, gq.scale, gq.rcp, neg_z, top_z);
+                        const float qz = fminf(fmaxf(e[j], neg_z), top_z);    // (q - z)
                         e[j] = __fmul_rn(__fsub_rn(__fmul_rn(qz, gq.scale), w), is[j]);
                     }
 #pragma unroll
