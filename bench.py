@@ -72,6 +72,32 @@ def src_sha(name):
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
 
+# ------------------------------------------------------------ multi-rank --
+
+def rank_layer(rank):
+    """Weak scaling across GPUs: rank r quantises and runs decoder layer r of
+    the workload (every layer's statistics, search, pack and matmuls are
+    independent), so the data path has no collective."""
+    return rank
+
+
+def max_over_ranks(values, device):
+    """Each timing's maximum over all ranks (one all-reduce of the timings,
+    outside the timed region); the values themselves on a single rank."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_value(bytes_per_rank_step, steps, max_ms, world):
+    """Whole-job GB/s: the bytes all ranks processed over the slowest rank's
+    time."""
+    return world * bytes_per_rank_step * steps / (max_ms * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------- clocks --
 
 class ClockSampler:
@@ -139,7 +165,7 @@ def run_ours(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    layer = rank            # each rank quantises and runs its own layer (weak scaling)
+    layer = rank_layer(rank)
     projs = []
     for j, (name, N, K) in enumerate(sg.LLAMA7B_DECODE_PROJ):
         W, Xc, Xm, _ = sg.layer_inputs(layer, j, N, K, T_CAL, M=1)
@@ -255,14 +281,10 @@ def run_ours(args, rank, world):
         per_gemv.append(statistics.median(ts))
 
     # max over ranks of the timed region and the GEMV segment
-    gemv_ms = st["gemv"]
-    if world > 1:
-        t = torch.tensor([total_ms, gemv_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, gemv_ms = float(t[0]), float(t[1])
+    total_ms, gemv_ms = max_over_ranks([total_ms, st["gemv"]], dev)
     bytes_step = sum(gemv_bytes(p["N"], p["K"]) for p in projs)
     flop_step = sum(search_flop(p["N"], p["K"]) for p in projs)
-    value = world * bytes_step * args.steps / (gemv_ms * 1e-3) / 1e9
+    value = job_value(bytes_step, args.steps, gemv_ms, world)
     peaks, peak_src = load_peaks()
     search_tf = flop_step * args.steps / (st["search"] * 1e-3) / 1e12
     gemv_gbs = bytes_step * args.steps / (st["gemv"] * 1e-3) / 1e9
@@ -426,14 +448,9 @@ def run_e2e(args, projs, dev, stream, world):
         step()
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / n
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t[0])
+    ms = max_over_ranks([a.elapsed_time(b) / n], dev)[0]
     bytes_step = sum(gemv_bytes(p["N"], p["K"]) for p in projs)
-    return {"value": round(world * bytes_step / (ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+    return {"value": round(job_value(bytes_step, 1, ms, world), 3), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
             "steps": n,
             "basis": "decode-matmul algorithmic bytes / whole-step time with host buffers "

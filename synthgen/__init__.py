@@ -152,6 +152,23 @@ LLAMA7B_LAYER_LINEARS = (  # (name, N, K)
 )
 
 
+# A LLaMA-7B-shaped decoder layer's linears read four distinct inputs:
+# q, k, v the attention input; o the attention output; gate, up the MLP
+# input; down the MLP hidden state.  (input name, K) per input, and the
+# input index of each linear in LLAMA7B_LAYER_LINEARS.
+LLAMA7B_LAYER_INPUTS = (("attn_in", 4096), ("attn_out", 4096), ("mlp_in", 4096),
+                        ("mlp_hidden", 11008))
+LLAMA7B_LINEAR_INPUT = (0, 0, 0, 1, 2, 2, 3)
+
+
+def layer_activations(layer: int, index: int, T: int, K: int) -> np.ndarray:
+    """Calibration activations of input ``index`` of decoder ``layer``: fp16
+    ``[T, K]`` N(0,1) with the input's own 1% outlier channels x20 (seeds
+    offset by 8 so they never collide with a linear's own seeds)."""
+    ch = outlier_channels(layer_seed(SEED_CHANNELS, layer, 8 + index), K)
+    return gen_acts(layer_seed(SEED_XCAL, layer, 8 + index), T, K, ch)
+
+
 def layer_inputs(layer: int, linear: int, N: int, K: int, T_cal: int,
                  M: int = 0, sigma: float = 0.02):
     """The seeded inputs of one linear layer.

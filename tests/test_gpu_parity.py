@@ -346,3 +346,25 @@ def test_decode_chain_early_weights(wb, orc):
         wb.sync_status()
     finally:
         wb.set_weight_prefetch(False)
+
+
+def test_shared_input_search_qkv(wb, orc):
+    """Projections that read the same input (q, k, v) share one s, searched
+    on their concatenated weight with the shared calibration activations
+    (the scale is per input channel, so all three use it).  The fused search
+    matches the oracle, and packing each projection with the shared s gives
+    exactly the rows of the fused pack."""
+    K, T = 1024, 256
+    Ws = [sg.layer_inputs(40, j, 384, K, 0)[0] for j in range(3)]
+    _, X, _, _ = sg.layer_inputs(40, 0, 8, K, T)
+    Wqkv = np.concatenate(Ws, axis=0)
+    mse, best = _search_check(wb, orc, Wqkv, X)
+    m = orc.act_mean(orc.act_stats(X), T)
+    s = orc.candidate_scales(m, orc.ALPHA_GRID[best])
+    fq, fs, fz = wb.pack_int4(dev(Wqkv), dev(s))
+    fq, fs, fz = u32(fq), u16(fs), u16(fz)
+    for j, W in enumerate(Ws):
+        q, sc, ze = wb.pack_int4(dev(W), dev(s))
+        rows = slice(384 * j, 384 * (j + 1))
+        assert np.array_equal(u32(q), fq[rows]) and np.array_equal(u16(sc), fs[rows])
+        assert np.array_equal(u16(ze), fz[rows])
