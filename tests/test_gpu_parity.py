@@ -166,6 +166,19 @@ def _search_check(wb, orc, W, X, alphas=None):
     return mse, best
 
 
+def test_search_nonfinite_flag(wb):
+    """A NaN weight reaches the status word through the search too."""
+    W, X, _, _ = sg.layer_inputs(16, 0, 128, 256, 32)
+    W = W.copy()
+    W[70, 200] = np.nan
+    m = wb.act_mean(wb.act_stats(dev(X)), 32)
+    wb.search_scale(dev(W), dev(X), m)
+    with pytest.raises(wb.AwqError) as e:
+        wb.sync_status()
+    assert e.value.code == 8
+    wb.sync_status()
+
+
 @pytest.mark.parametrize("N,K,T", [(128, 128, 1), (256, 512, 300), (136, 256, 64),
                                    (384, 384, 700)])
 def test_search_parity_small(wb, orc, N, K, T):

@@ -32,6 +32,20 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     return t;
 }
 
+// min / max that return NaN when either input is NaN (fminf / fmaxf ignore
+// NaN), so a lane's reduction of its values is non-finite exactly when one
+// of them is.
+__device__ __forceinline__ float fmin_nan(float a, float b) {
+    float r;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
 __device__ __forceinline__ float warp_min(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -72,51 +72,87 @@ __global__ void __launch_bounds__(kCandThreads)
     }
 }
 
-// One warp per (row, group): quantise 128 scaled weights and write 16 words,
-// the group's fp16 scale and fp16 zero-point.
+// Eight lanes per (row, group), four row-groups per warp: lane c holds the
+// 16 channels 16c..16c+15 of its row-group, forms the group's range with
+// three shuffle rounds, rounds its 16 levels with the branch-free exact
+// quotient (the same levels as the search producer's), and writes its two
+// packed words; the eight lanes of a row-group write its 64 bytes at once.
 __global__ void __launch_bounds__(256)
     pack_int4_kernel(const uint16_t* __restrict__ W, int64_t N, int64_t K, int64_t ldw,
                      const float* __restrict__ s, uint32_t* __restrict__ qweight,
                      uint16_t* __restrict__ scales, uint16_t* __restrict__ zeros,
                      unsigned* status) {
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, c = lane & 7, rg = lane >> 3;
     const int64_t G = K / kGroup;
     const int64_t total = N * G;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
     bool bad = false;
-    for (int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < total;
-         item += nwarps) {
-        const int64_t n = item / G, g = item - n * G;
-        const int64_t k0 = g * kGroup + 4 * lane;
-        uint2 raw = __ldg(reinterpret_cast<const uint2*>(W + n * ldw + k0));
-        float4 sv = s ? __ldg(reinterpret_cast<const float4*>(s + k0)) : make_float4(1, 1, 1, 1);
-        float wp[4];
-        wp[0] = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(raw.x & 0xFFFFu))), sv.x);
-        wp[1] = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(raw.x >> 16))), sv.y);
-        wp[2] = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(raw.y & 0xFFFFu))), sv.z);
-        wp[3] = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(raw.y >> 16))), sv.w);
+    // every lane runs the same number of iterations (the shuffles and the
+    // vote need the whole warp); lanes past the end work on a clamped item
+    for (int64_t base = warp0 * 4; base < total; base += nwarps * 4) {
+        const int64_t item = base + rg;
+        const bool live = item < total;
+        const int64_t it = live ? item : total - 1;
+        const int64_t n = it / G, g = it - n * G;
+        const int64_t k0 = g * kGroup + 16 * c;
+        const uint4* wp4 = reinterpret_cast<const uint4*>(W + n * ldw + k0);
+        const uint4 r0 = __ldg(wp4), r1 = __ldg(wp4 + 1);
+        float4 sv[4];
+        if (s) {
+            const float4* sp = reinterpret_cast<const float4*>(s + k0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sv[j] = __ldg(sp + j);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sv[j] = make_float4(1.f, 1.f, 1.f, 1.f);
+        }
+        const uint32_t wr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        const float* sf = reinterpret_cast<const float*>(sv);
+        float wp[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const uint32_t h = (wr[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+            wp[e] = __fmul_rn(__half2float(__ushort_as_half((unsigned short)h)), sf[e]);
+        }
         float lo = wp[0], hi = wp[0];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            bad |= !isfinite(wp[e]);
-            lo = fminf(lo, wp[e]);
-            hi = fmaxf(hi, wp[e]);
+        for (int e = 1; e < 16; ++e) {
+            lo = fmin_nan(lo, wp[e]);
+            hi = fmax_nan(hi, wp[e]);
         }
-        GroupQuant gq = group_quant_params(lo, hi);
-        bad |= !gq.finite;
-        uint32_t v = 0;
+        // this lane's 16 values: NaN or Inf makes lo or hi non-finite
+        const bool lane_bad = !(isfinite(lo) && isfinite(hi));
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v |= (uint32_t)quant_level(wp[e], gq) << (4 * e);
-        uint32_t other = __shfl_xor_sync(0xffffffffu, v, 1);
-        if ((lane & 1) == 0) qweight[n * (K / 8) + g * 16 + (lane >> 1)] = v | (other << 16);
-        if (lane == 0) {
-            scales[n * G + g] = __half_as_ushort(gq.scale_h);
-            zeros[n * G + g] = __half_as_ushort(__float2half_rn(gq.zf));
+        for (int o = 1; o < 8; o <<= 1) {
+            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+        const GroupQuant gq = group_quant_from_range(lo, hi);
+        if (live) bad |= lane_bad || !gq.finite;
+        float rt[16];
+        rint_quot8(wp, gq.scale, gq.rcp, rt);
+        rint_quot8(wp + 8, gq.scale, gq.rcp, rt + 8);
+        uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            w0 |= (uint32_t)fminf(fmaxf(__fadd_rn(rt[e], gq.zf), 0.0f), 15.0f) << (4 * e);
+            w1 |= (uint32_t)fminf(fmaxf(__fadd_rn(rt[e + 8], gq.zf), 0.0f), 15.0f) << (4 * e);
+        }
+        if (live) {
+            *reinterpret_cast<uint2*>(qweight + n * (K / 8) + g * 16 + 2 * c) = make_uint2(w0, w1);
+            if (c == 0) {
+                scales[n * G + g] = __half_as_ushort(gq.scale_h);
+                zeros[n * G + g] = __half_as_ushort(__float2half_rn(gq.zf));
+            }
         }
     }
     if (bad) set_status(status, kStatusNonFinite);
 }
 
+// mse[a] = (sum of alpha a's partials) / (T N): one warp per alpha, lane-
+// strided fp64 sums added in a fixed butterfly order (deterministic); then
+// the first argmin and its candidate scales.
 __global__ void __launch_bounds__(256)
     search_finalize_kernel(const double* __restrict__ partials, int n_alpha, int64_t n_part,
                            int64_t T, int64_t N, int64_t K, const float* __restrict__ s_alpha,
@@ -125,11 +161,17 @@ __global__ void __launch_bounds__(256)
     __shared__ double smse[64];
     __shared__ int sbest;
     const double denom = (double)T * (double)N;
-    for (int a = threadIdx.x; a < n_alpha; a += blockDim.x) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int a = warp; a < n_alpha; a += blockDim.x >> 5) {
+        const double* pa = partials + (int64_t)a * n_part;
         double acc = 0.0;
-        for (int64_t i = 0; i < n_part; ++i) acc += partials[(int64_t)a * n_part + i];
-        smse[a] = acc / denom;
-        if (mse) mse[a] = acc / denom;
+        for (int64_t i = lane; i < n_part; i += 32) acc += pa[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) {
+            smse[a] = acc / denom;
+            if (mse) mse[a] = acc / denom;
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -140,8 +182,9 @@ __global__ void __launch_bounds__(256)
         *best_idx = b;
     }
     __syncthreads();
-    const float* src = s_alpha + (int64_t)sbest * K;
-    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) s_out[k] = src[k];
+    const float4* src = reinterpret_cast<const float4*>(s_alpha + (int64_t)sbest * K);
+    float4* dst = reinterpret_cast<float4*>(s_out);
+    for (int64_t k = threadIdx.x; k < K / 4; k += blockDim.x) dst[k] = src[k];
 }
 
 }  // namespace
@@ -165,8 +208,8 @@ cudaError_t launch_pack_int4(const uint16_t* W, int64_t N, int64_t K, int64_t ld
                              int num_sms, cudaStream_t st) {
     const int64_t items = N * (K / kGroup);
     if (items == 0) return cudaSuccess;
-    int64_t blocks = (items + 7) / 8;
-    const int64_t cap = (int64_t)num_sms * 16;
+    int64_t blocks = (items + 31) / 32;               // 8 warps x 4 row-groups
+    const int64_t cap = (int64_t)num_sms * 8;
     if (blocks > cap) blocks = cap;
     pack_int4_kernel<<<(unsigned)blocks, 256, 0, st>>>(W, N, K, ldw, s, qweight, scales, zeros,
                                                        status);

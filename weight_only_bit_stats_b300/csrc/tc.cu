@@ -387,15 +387,17 @@ __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, i
                 float lo = wp[0], hi = wp[0];
 #pragma unroll
                 for (int e = 1; e < 16; ++e) {
-                    lo = fminf(lo, wp[e]);
-                    hi = fmaxf(hi, wp[e]);
+                    lo = fmin_nan(lo, wp[e]);
+                    hi = fmax_nan(hi, wp[e]);
                 }
+                // this lane's 16 values: NaN or Inf makes lo or hi non-finite
+                const bool lane_bad = !(isfinite(lo) && isfinite(hi));
 #pragma unroll
                 for (int o = 1; o < 8; o <<= 1) {
                     lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
                     hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
                 }
-                bad |= !(isfinite(lo) && isfinite(hi));
+                bad |= lane_bad;
                 const GroupQuant gq = group_quant_from_range(lo, hi);
                 bad |= !gq.finite;
                 const float neg_z = -gq.zf, top_z = 15.0f - gq.zf;
