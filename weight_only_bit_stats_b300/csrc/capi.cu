@@ -319,19 +319,56 @@ awq_status awq_pack_int4(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, c
     return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
 }
 
+}  // extern "C"
+
+namespace {
+
+// K splits of the tensor-core GEMM: the count that minimises the modelled
+// time, waves x (groups per split) x (one group of one 128 x 256 tile,
+// about 1 us on B300) plus the split partials' extra traffic (written and
+// read once, fp32, at about 5 TB/s).  Splitting pays only for under-filled
+// grids with long K (e.g. 64 output tiles with K = 28672).
+int gemm_k_splits(int64_t M, int64_t N, int64_t K, int num_sms) {
+    if (M <= 16 || num_sms <= 0) return 1;
+    const int64_t G = K / AWQ_GROUP;
+    const int64_t tiles = ((N + awq::kTcRows - 1) / awq::kTcRows) *
+                          ((M + awq::kGemmTokensPerItem - 1) / awq::kGemmTokensPerItem);
+    int best = 1;
+    double best_t = 1e300;
+    for (int ks = 1; ks <= 8; ++ks) {
+        if (G / ks < 4) break;
+        const int64_t waves = (tiles * ks + num_sms - 1) / num_sms;
+        const double t = (double)waves * ((double)G / ks) * 1e-6 +
+                         (ks > 1 ? 2.0 * ks * (double)M * (double)N * 4.0 / 5e12 : 0.0);
+        if (t < best_t * 0.97) {       // a split must win clearly
+            best_t = t;
+            best = ks;
+        }
+    }
+    return best;
+}
+
+int current_num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+}  // namespace
+
+extern "C" {
+
 size_t w4a16_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
-    (void)M;
-    (void)N;
-    (void)K;
-    return 0;
+    if (M <= 16 || N <= 0 || K <= 0 || K % AWQ_GROUP) return 0;
+    const int ks = gemm_k_splits(M, N, K, current_num_sms());
+    return ks > 1 ? (size_t)ks * (size_t)M * (size_t)N * sizeof(float) : 0;
 }
 
 awq_status w4a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx, const uint32_t* qweight,
                       const uint16_t* scales, const uint16_t* zeros, int64_t N, int group,
                       uint16_t* Y, int64_t ldy, void* workspace, size_t ws_bytes,
                       awq_stream_t stream) {
-    (void)workspace;
-    (void)ws_bytes;
     if (M < 0 || N < 0 || K < 0) return fail(AWQ_ERR_INVALID_ARG, "w4a16_gemm: negative size");
     if (M == 0 || N == 0) return AWQ_OK;
     if (!X || !qweight || !scales || !zeros || !Y)
@@ -373,7 +410,18 @@ awq_status w4a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx, cons
         p.Y = Y;
         p.ldy = ldy;
         p.status = d->status;
+        p.k_splits = gemm_k_splits(M, N, K, d->num_sms);
+        p.n_items *= p.k_splits;
+        if (p.k_splits > 1) {
+            const size_t need = (size_t)p.k_splits * (size_t)M * (size_t)N * sizeof(float);
+            if (!workspace || ws_bytes < need || !aligned16(workspace))
+                return fail(AWQ_ERR_WORKSPACE, "w4a16_gemm: workspace missing or too small "
+                                               "(see w4a16_gemm_workspace_size)");
+            p.ws_partial = static_cast<float*>(workspace);
+        }
         e = awq::launch_tc_gemm(map, p, d->num_sms, st);
+        if (e == cudaSuccess && p.k_splits > 1)
+            e = awq::launch_splitk_reduce(p.ws_partial, p.k_splits, M, N, Y, ldy, d->num_sms, st);
     }
     return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
 }

@@ -66,6 +66,8 @@ struct TcParams {
     const uint16_t* zeros;
     uint16_t* Y;
     int64_t ldy;
+    int k_splits;          // K split over this many items per output tile (1: none)
+    float* ws_partial;     // k_splits > 1: fp32 partials [k_splits][rows_tok][N]
     // search
     const uint16_t* W;
     int64_t ldw;
@@ -82,6 +84,9 @@ constexpr int kSearchTokensPerItem = 512;
 
 cudaError_t launch_tc_gemm(const CUtensorMap& mapX, const TcParams& p, int num_sms,
                            cudaStream_t st);
+// Y = fp16(sum over splits of ws_partial), the splits added in order.
+cudaError_t launch_splitk_reduce(const float* ws_partial, int k_splits, int64_t M, int64_t N,
+                                 uint16_t* Y, int64_t ldy, int num_sms, cudaStream_t st);
 cudaError_t launch_tc_search(const CUtensorMap& mapX, const TcParams& p, int num_sms,
                              cudaStream_t st);
 

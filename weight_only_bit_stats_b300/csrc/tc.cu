@@ -64,20 +64,31 @@ constexpr size_t kSmemBytes = 1024 /*align slack*/ + kNA * kAStage + kNB * kBSta
 
 struct Item {
     int n_tile, t_tile, alpha;
+    int split, g0, g1;                 // GEMM split-K: this item's groups [g0, g1)
 };
 
 template <int MODE>
 __device__ __forceinline__ Item decode_item(int item, const TcParams& p) {
     Item it;
-    if (MODE == kModeGemm) {           // consecutive CTAs share the activation tile
-        it.n_tile = item % p.n_tiles;
-        it.t_tile = item / p.n_tiles;
+    if (MODE == kModeGemm) {
+        // consecutive CTAs share the weight tile: the token tiles of one
+        // weight tile run together, so its packed words leave DRAM once and
+        // the activations (a few tens of MB) stay in L2
+        it.t_tile = item % p.t_tiles;
+        const int rest = item / p.t_tiles;
+        it.n_tile = rest % p.n_tiles;
+        it.split = rest / p.n_tiles;
         it.alpha = 0;
+        it.g0 = (int)((int64_t)it.split * p.G / p.k_splits);
+        it.g1 = (int)((int64_t)(it.split + 1) * p.G / p.k_splits);
     } else {                           // consecutive CTAs share the weight tile
         it.alpha = item % p.n_alpha;
         const int rest = item / p.n_alpha;
         it.t_tile = rest % p.t_tiles;
         it.n_tile = rest / p.t_tiles;
+        it.split = 0;
+        it.g0 = 0;
+        it.g1 = p.G;
     }
     return it;
 }
@@ -95,20 +106,22 @@ template <int MODE>
 __device__ void role_tma(const CUtensorMap* mapX, const TcParams& p, uint8_t* Bs, SmemCtl* ctl) {
     constexpr int H = Cfg<MODE>::kHalves;
     volatile int* abort = &ctl->abort;
+    // the activation tiles are re-read by every weight tile: keep them in L2
+    const uint64_t pol = l2_policy_evict_last();
     uint32_t b_iter = 0;
     for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
         const Item it = decode_item<MODE>(item, p);
         const int t0 = it.t_tile * kTcTokens * H;
-        for (int g = 0; g < p.G; ++g) {
+        for (int g = it.g0; g < it.g1; ++g) {
             for (int h = 0; h < H; ++h) {
                 const int st = b_iter % kNB;
                 const uint32_t ph = (b_iter / kNB) & 1u;
                 if (!mbar_wait(&ctl->b_empty[st], ph ^ 1u, abort, p.status)) goto drain;
                 mbar_arrive_expect_tx(&ctl->b_full[st], kBStage);
                 uint8_t* dst = Bs + st * kBStage;
-                tma_load_2d(dst, mapX, &ctl->b_full[st], g * kGroup, t0 + h * kTcTokens);
-                tma_load_2d(dst + kBSub, mapX, &ctl->b_full[st], g * kGroup + 64,
-                            t0 + h * kTcTokens);
+                tma_load_2d_hint(dst, mapX, &ctl->b_full[st], g * kGroup, t0 + h * kTcTokens, pol);
+                tma_load_2d_hint(dst + kBSub, mapX, &ctl->b_full[st], g * kGroup + 64,
+                                 t0 + h * kTcTokens, pol);
                 ++b_iter;
             }
         }
@@ -130,7 +143,8 @@ __device__ void role_mma(const TcParams& p, uint8_t* As, uint8_t* Bs, SmemCtl* c
     volatile int* abort = &ctl->abort;
     uint32_t a_iter = 0, b_iter = 0, acc_iter = 0;
     for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
-        for (int g = 0; g < p.G; ++g) {
+        const Item it = decode_item<MODE>(item, p);
+        for (int g = it.g0; g < it.g1; ++g) {
             const int sa = a_iter % kNA;
             if (!mbar_wait(&ctl->a_full[sa], (a_iter / kNA) & 1u, abort, p.status)) goto out;
             tc_fence_after();
@@ -138,7 +152,7 @@ __device__ void role_mma(const TcParams& p, uint8_t* As, uint8_t* Bs, SmemCtl* c
             for (int h = 0; h < H; ++h) {
                 const uint32_t slot_iter = acc_iter + h;
                 const int slot = slot_iter & 1;
-                if (g == 0) {
+                if (g == it.g0) {
                     if (!mbar_wait(&ctl->acc_empty[slot], ((slot_iter >> 1) & 1u) ^ 1u, abort,
                                    p.status))
                         goto out;
@@ -154,7 +168,7 @@ __device__ void role_mma(const TcParams& p, uint8_t* As, uint8_t* Bs, SmemCtl* c
                     const uint32_t sub = ks >> 2, koff = (ks & 3) * 32;
                     const uint64_t ad = umma_desc_sw128(a_base + sub * kASub + koff);
                     const uint64_t bd = umma_desc_sw128(b_base + sub * kBSub + koff);
-                    umma_f16(d, ad, bd, idesc, (g > 0 || ks > 0) ? 1u : 0u);
+                    umma_f16(d, ad, bd, idesc, (g > it.g0 || ks > 0) ? 1u : 0u);
                 }
                 umma_commit(&ctl->b_empty[sb]);
                 ++b_iter;
@@ -193,11 +207,22 @@ __device__ void role_epilogue(const TcParams& p, SmemCtl* ctl, uint32_t tmem, in
                 tmem_ld32(taddr + c * 32, v);
                 if (MODE == kModeGemm) {
                     if (n < p.N) {
+                        if (p.k_splits == 1) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int64_t tok = tok0 + c * 32 + j;
-                            if (tok < p.rows_tok)
-                                p.Y[tok * p.ldy + n] = __half_as_ushort(__float2half_rn(v[j]));
+                            for (int j = 0; j < 32; ++j) {
+                                const int64_t tok = tok0 + c * 32 + j;
+                                if (tok < p.rows_tok)      // streaming: Y does not evict X
+                                    __stcs(reinterpret_cast<unsigned short*>(p.Y) + tok * p.ldy + n,
+                                           __half_as_ushort(__float2half_rn(v[j])));
+                            }
+                        } else {
+                            // fp32 partial of this split, laid out like Y
+                            float* wsp = p.ws_partial + (int64_t)it.split * p.rows_tok * p.N + n;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const int64_t tok = tok0 + c * 32 + j;
+                                if (tok < p.rows_tok) __stcs(wsp + tok * p.N, v[j]);
+                            }
                         }
                     }
                 } else {
@@ -268,14 +293,14 @@ __device__ void role_prod_gemm(const TcParams& p, uint8_t* As, SmemCtl* ctl, int
         uint16_t csc = 0, cze = 0;
         if (valid) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) cur[j] = __ldg(qrow + j);
-            csc = __ldg(srow);
-            cze = __ldg(zrow);
+            for (int j = 0; j < 4; ++j) cur[j] = __ldg(qrow + (int64_t)it.g0 * 4 + j);
+            csc = __ldg(srow + it.g0);
+            cze = __ldg(zrow + it.g0);
         }
-        for (int g = 0; g < p.G; ++g) {
+        for (int g = it.g0; g < it.g1; ++g) {
             uint4 nxt[4];
             uint16_t nsc = 0, nze = 0;
-            if (valid && g + 1 < p.G) {
+            if (valid && g + 1 < it.g1) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) nxt[j] = __ldg(qrow + (int64_t)(g + 1) * 4 + j);
                 nsc = __ldg(srow + g + 1);
@@ -310,7 +335,7 @@ __device__ void role_prod_gemm(const TcParams& p, uint8_t* As, SmemCtl* ctl, int
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->a_full[st]);
             ++a_iter;
-            if (valid && g + 1 < p.G) {
+            if (valid && g + 1 < it.g1) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) cur[j] = nxt[j];
                 csc = nsc;
@@ -501,7 +526,29 @@ cudaError_t launch_tc(const CUtensorMap& mapX, const TcParams& p, int num_sms, c
     return cudaGetLastError();
 }
 
+__global__ void __launch_bounds__(256)
+    splitk_reduce_kernel(const float* __restrict__ ws, int k_splits, int64_t M, int64_t N,
+                         uint16_t* __restrict__ Y, int64_t ldy) {
+    const int64_t per = M * N;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < per; i += stride) {
+        float acc = ws[i];
+        for (int s = 1; s < k_splits; ++s) acc += ws[(int64_t)s * per + i];
+        const int64_t m = i / N, n = i - m * N;
+        Y[m * ldy + n] = __half_as_ushort(__float2half_rn(acc));
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_splitk_reduce(const float* ws_partial, int k_splits, int64_t M, int64_t N,
+                                 uint16_t* Y, int64_t ldy, int num_sms, cudaStream_t st) {
+    const int64_t total = M * N;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > (int64_t)num_sms * 16) blocks = (int64_t)num_sms * 16;
+    splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(ws_partial, k_splits, M, N, Y, ldy);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_tc_gemm(const CUtensorMap& mapX, const TcParams& p, int num_sms,
                            cudaStream_t st) {
