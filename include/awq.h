@@ -174,14 +174,37 @@ awq_status awq_pack_int4(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
  *   qweight, scales, zeros: as written by awq_pack_int4 for an [N, K] weight.
  *   Y        [M, N] fp16, leading dimension ldy (>= N).
  * M <= 16 runs the decode kernel (packed weights streamed once, dequantised
- * in registers); M > 16 runs the tcgen05 tensor-core kernel.
- * workspace >= w4a16_gemm_workspace_size(M, N, K) bytes (may be 0/NULL when
- * that size is 0).  K % 128 == 0, N % 8 == 0, group == 128. */
+ * in registers); M > 16 runs the tcgen05 tensor-core kernel, with K split
+ * over several CTAs (fp32 partials in the workspace, added in order) when
+ * the grid would otherwise be under-filled.
+ * workspace >= w4a16_gemm_workspace_size(M, N, K) bytes on the device that
+ * runs the call (may be 0/NULL when that size is 0; 16-byte aligned).
+ * K % 128 == 0, N % 8 == 0, group == 128. */
 awq_status w4a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
                       const uint32_t* qweight, const uint16_t* scales, const uint16_t* zeros,
                       int64_t N, int group, uint16_t* Y, int64_t ldy, void* workspace,
                       size_t ws_bytes, awq_stream_t stream);
 size_t w4a16_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/* ---- dequantise-fused matmul with the input scaling fused -----------------
+ * The AWQ page's scaling trick divides each input channel by s (third
+ * paragraph); the OpenAlex record's abstract names kernel fusion.  Here the
+ * division is part of the matmul:
+ *   Y = fp16(fp32(X) * inv_s) deq(Wq)^T,
+ * each scaled activation rounded once to fp32 and once to fp16, then used
+ * exactly as w4a16_gemm uses X (so the result equals w4a16_gemm on those
+ * fp16 values).  For M <= 16 the scaling happens as the decode kernel stages
+ * its activations; for M > 16 a pre-pass writes the scaled activations into
+ * the workspace.
+ *   X      [M, K] fp16 unscaled, leading dimension ldx.
+ *   inv_s  [K] fp32 device, 1/s per input channel (16-byte aligned).
+ *   other arguments as w4a16_gemm; workspace >=
+ *   w4a16_gemm_scaled_workspace_size(M, N, K) bytes. */
+awq_status w4a16_gemm_scaled(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
+                             const float* inv_s, const uint32_t* qweight, const uint16_t* scales,
+                             const uint16_t* zeros, int64_t N, int group, uint16_t* Y, int64_t ldy,
+                             void* workspace, size_t ws_bytes, awq_stream_t stream);
+size_t w4a16_gemm_scaled_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /* Overlap of back-to-back decode matmuls (M <= 16).  Every decode launch
  * lets the next kernel in the stream start beside it (programmatic dependent

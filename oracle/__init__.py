@@ -72,6 +72,7 @@ def _lib():
         lib.awqo_d2h_array.argtypes = [_ptr, _i64, _ptr]
         lib.awqo_w4a16_pairs.argtypes = [_ptr, _i64, _i64, _ptr, _ptr, _ptr, _i64,
                                          _ptr, _ptr, _ptr]
+        lib.awqo_scale_activations.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
         _LIB = lib
     return _LIB
 
@@ -288,6 +289,16 @@ def w4a16_pairs(X: np.ndarray, qweight: np.ndarray, scales: np.ndarray,
     _lib().awqo_w4a16_pairs(_p(xb), K, K, _p(np.ascontiguousarray(qweight, dtype=np.uint32)),
                             _p(_bits(scales)), _p(_bits(zeros)), ms.size, _p(ms), _p(ns),
                             _p(out))
+    return out
+
+
+def scale_activations(X: np.ndarray, inv_s: np.ndarray) -> np.ndarray:
+    """The matmul's input scaling: fp16(fp32(X * inv_s)) per element (bits)."""
+    xb = _bits(X)
+    M, K = xb.shape
+    inv = np.ascontiguousarray(inv_s, dtype=np.float32)
+    out = np.empty((M, K), dtype=np.uint16)
+    _lib().awqo_scale_activations(_p(xb), M, K, _p(inv), _p(out))
     return out
 
 

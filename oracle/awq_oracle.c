@@ -264,3 +264,14 @@ void awqo_w4a16_pairs(const uint16_t* X, int64_t ldx, int64_t K,
 void awqo_d2h_array(const double* x, int64_t n, uint16_t* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = awqo_d2h_rn(x[i]);
 }
+
+/* Input scaling of the matmul: Xs[m,k] = fp16_rn(fp32(X[m,k] * inv_s[k])),
+ * the product exact in fp64 and rounded once to fp32, then once to fp16. */
+void awqo_scale_activations(const uint16_t* X, int64_t M, int64_t K, const float* inv_s,
+                            uint16_t* Xs) {
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) {
+            float v = (float)(awqo_h2d(X[m * K + k]) * (double)inv_s[k]);
+            Xs[m * K + k] = awqo_d2h_rn((double)v);
+        }
+}

@@ -381,3 +381,22 @@ def test_shared_input_search_qkv(wb, orc):
         rows = slice(384 * j, 384 * (j + 1))
         assert np.array_equal(u32(q), fq[rows]) and np.array_equal(u16(sc), fs[rows])
         assert np.array_equal(u16(ze), fz[rows])
+
+
+@pytest.mark.parametrize("M", [1, 5, 9, 16, 64, 300])
+def test_gemm_scaled_fused_input(wb, orc, M):
+    """w4a16_gemm_scaled: the input scaling X * (1/s) fused into the matmul
+    equals the plain matmul on the oracle's scaled activations, bit for
+    bit, and the oracle's fp64 product within 2e-3."""
+    N, K = 520, 2304
+    W, Xc, X, _ = sg.layer_inputs(17, 0, N, K, 64, M=M)
+    m = orc.act_mean(orc.act_stats(Xc), 64)
+    s = orc.candidate_scales(m, 0.45)
+    inv = (np.float32(1) / s).astype(np.float32)
+    rq, rs, rz = orc.pack_int4(W, s)
+    qw, sc, ze = dev(rq.view(np.int32)), dev(rs.view(np.float16)), dev(rz.view(np.float16))
+    Xs = orc.scale_activations(X, inv)
+    y_fused = host(wb.w4a16_gemm_scaled(dev(X), dev(inv), qw, sc, ze))
+    y_plain = host(wb.w4a16_gemm(dev(Xs.view(np.float16)), qw, sc, ze))
+    assert np.array_equal(y_fused.view(np.uint16), y_plain.view(np.uint16))
+    assert rel_err(y_fused, orc.w4a16_gemm(Xs, rq, rs, rz)) <= GEMM_TOL

@@ -439,3 +439,16 @@ def test_search_tie_goes_to_lowest_alpha(oracle_mod):
     m = np.full(256, 0.8)
     _, mse, best = oracle_mod.search_scale(W, X, m, alphas=(0.3, 0.1, 0.2))
     assert mse[0] == mse[1] == mse[2] and best == 0
+
+
+def test_scale_activations_independent_route(oracle_mod):
+    """The matmul's input scaling fp16(fp32(x * inv_s)): numpy's IEEE float32
+    multiply and float16 conversion give the same bits."""
+    rng = np.random.default_rng(21)
+    X = (rng.standard_normal((7, 384)) * 3).astype(np.float16)
+    X[0, :5] = [0.0, -0.0, 65504.0, -6.1e-5, 1e-7]
+    inv = np.exp(rng.uniform(-3, 3, 384)).astype(np.float32)
+    got = oracle_mod.scale_activations(X, inv)
+    with np.errstate(over="ignore"):
+        ref = (X.astype(np.float32) * inv[None, :]).astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, ref)

@@ -21,7 +21,8 @@ import os
 import torch
 
 __all__ = ["AwqError", "lib", "act_stats", "act_mean", "candidate_scales", "search_scale",
-           "pack_int4", "w4a16_gemm", "set_weight_prefetch", "sync_status", "ALPHA_GRID",
+           "pack_int4", "w4a16_gemm", "w4a16_gemm_scaled", "set_weight_prefetch", "sync_status",
+           "ALPHA_GRID",
            "GROUP"]
 
 GROUP = 128
@@ -59,6 +60,9 @@ SIGNATURES = (
     ("awq_pack_int4", _int, [_p, _i64, _i64, _i64, _p, _int, _p, _p, _p, _p]),
     ("w4a16_gemm", _int, [_p, _i64, _i64, _i64, _p, _p, _p, _i64, _int, _p, _i64, _p, _sz, _p]),
     ("w4a16_gemm_workspace_size", _sz, [_i64, _i64, _i64]),
+    ("w4a16_gemm_scaled", _int, [_p, _i64, _i64, _i64, _p, _p, _p, _p, _i64, _int, _p, _i64, _p,
+                                 _sz, _p]),
+    ("w4a16_gemm_scaled_workspace_size", _sz, [_i64, _i64, _i64]),
     ("awq_set_weight_prefetch", _int, [_int]),
     ("awq_sync_status", _int, [_p]),
     ("awq_last_error_string", ctypes.c_char_p, []),
@@ -224,6 +228,28 @@ def w4a16_gemm(X: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, zer
                             zeros.data_ptr(), N, GROUP, Y.data_ptr(), _ld(Y),
                             ws.data_ptr() if ws is not None else None, ws_n, _stream(stream)),
            "w4a16_gemm")
+    return Y
+
+
+def w4a16_gemm_scaled(X: torch.Tensor, inv_s: torch.Tensor, qweight: torch.Tensor,
+                      scales: torch.Tensor, zeros: torch.Tensor,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y = fp16(X * inv_s) deq(Wq)^T with the input scaling fused, fp16 [M, N]."""
+    _dev(X, torch.float16, "X")
+    _dev(inv_s, torch.float32, "inv_s")
+    _dev(qweight, torch.int32, "qweight")
+    _dev(scales, torch.float16, "scales")
+    _dev(zeros, torch.float16, "zeros")
+    M, K = X.shape
+    N = qweight.shape[0]
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=X.device)
+    ws_n = lib().w4a16_gemm_scaled_workspace_size(M, N, K)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=X.device) if ws_n else None
+    _check(lib().w4a16_gemm_scaled(X.data_ptr(), M, K, _ld(X), inv_s.data_ptr(),
+                                   qweight.data_ptr(), scales.data_ptr(), zeros.data_ptr(), N,
+                                   GROUP, Y.data_ptr(), _ld(Y),
+                                   ws.data_ptr() if ws is not None else None, ws_n,
+                                   _stream(stream)), "w4a16_gemm_scaled")
     return Y
 
 

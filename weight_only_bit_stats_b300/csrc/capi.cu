@@ -365,10 +365,21 @@ size_t w4a16_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
     return ks > 1 ? (size_t)ks * (size_t)M * (size_t)N * sizeof(float) : 0;
 }
 
-awq_status w4a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx, const uint32_t* qweight,
-                      const uint16_t* scales, const uint16_t* zeros, int64_t N, int group,
-                      uint16_t* Y, int64_t ldy, void* workspace, size_t ws_bytes,
-                      awq_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Bytes the fused-scaling pre-pass needs in front of the GEMM's own
+// workspace (M > 16 only).
+size_t scaled_x_bytes(int64_t M, int64_t K) {
+    return M > 16 ? align256((size_t)M * (size_t)K * 2) : 0;
+}
+
+// w4a16_gemm and w4a16_gemm_scaled: inv_s null for the plain call.
+awq_status gemm_impl(const char* name, const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
+                     const float* inv_s, const uint32_t* qweight, const uint16_t* scales,
+                     const uint16_t* zeros, int64_t N, int group, uint16_t* Y, int64_t ldy,
+                     void* workspace, size_t ws_bytes, awq_stream_t stream) {
     if (M < 0 || N < 0 || K < 0) return fail(AWQ_ERR_INVALID_ARG, "w4a16_gemm: negative size");
     if (M == 0 || N == 0) return AWQ_OK;
     if (!X || !qweight || !scales || !zeros || !Y)
@@ -378,8 +389,10 @@ awq_status w4a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx, cons
     if (M > (1LL << 30) || N > (1LL << 30) || K > (1LL << 30))
         return fail(AWQ_ERR_SHAPE, "w4a16_gemm: size too large");
     if (!aligned16(X) || !aligned16(qweight) || (reinterpret_cast<uintptr_t>(Y) & 1u) ||
-        (reinterpret_cast<uintptr_t>(scales) & 1u) || (reinterpret_cast<uintptr_t>(zeros) & 1u))
-        return fail(AWQ_ERR_ALIGN, "w4a16_gemm: X and qweight must be 16-byte aligned");
+        (reinterpret_cast<uintptr_t>(scales) & 1u) || (reinterpret_cast<uintptr_t>(zeros) & 1u) ||
+        (inv_s && !aligned16(inv_s)))
+        return fail(AWQ_ERR_ALIGN, "w4a16_gemm: X, qweight (and inv_s) must be 16-byte aligned");
+    (void)name;
     DevInfo* d = nullptr;
     awq_status s = device_info(&d);
     if (s) return s;
@@ -390,11 +403,30 @@ awq_status w4a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx, cons
         s = make_qweight_map(&map, qweight, N, K);
         if (s) return s;
         awq::GemvParams p = {X, ldx, (int)M, qweight, scales, zeros, N, K, (int)(K / AWQ_GROUP),
-                             Y, ldy, d->status, g_early_weights.load(std::memory_order_relaxed)};
+                             Y, ldy, d->status, g_early_weights.load(std::memory_order_relaxed),
+                             inv_s};
         e = awq::launch_gemv(map, p, d->num_sms, st);
     } else {
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        const size_t xs_bytes = inv_s ? scaled_x_bytes(M, K) : 0;
+        const int k_splits = gemm_k_splits(M, N, K, d->num_sms);
+        const size_t part_bytes =
+            k_splits > 1 ? (size_t)k_splits * (size_t)M * (size_t)N * sizeof(float) : 0;
+        if ((xs_bytes + part_bytes) > 0 &&
+            (!workspace || ws_bytes < xs_bytes + part_bytes || !aligned16(workspace)))
+            return fail(AWQ_ERR_WORKSPACE, "w4a16_gemm: workspace missing or too small "
+                                           "(see w4a16_gemm_workspace_size)");
+        const uint16_t* Xa = X;
+        int64_t lda = ldx;
+        if (inv_s) {   // pre-pass: fp16(X * inv_s) into the workspace
+            uint16_t* Xs = reinterpret_cast<uint16_t*>(ws);
+            e = awq::launch_scale_x(X, M, K, ldx, inv_s, Xs, d->num_sms, st);
+            if (e != cudaSuccess) return cuda_fail(e);
+            Xa = Xs;
+            lda = K;
+        }
         CUtensorMap map;
-        s = make_act_map(&map, X, M, K, ldx);
+        s = make_act_map(&map, Xa, M, K, lda);
         if (s) return s;
         awq::TcParams p = {};
         p.N = (int)N;
@@ -403,27 +435,46 @@ awq_status w4a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx, cons
         p.rows_tok = (int)M;
         p.n_tiles = (int)((N + awq::kTcRows - 1) / awq::kTcRows);
         p.t_tiles = (int)((M + awq::kGemmTokensPerItem - 1) / awq::kGemmTokensPerItem);
-        p.n_items = p.n_tiles * p.t_tiles;
+        p.k_splits = k_splits;
+        p.n_items = p.n_tiles * p.t_tiles * k_splits;
         p.qw = qweight;
         p.scales = scales;
         p.zeros = zeros;
         p.Y = Y;
         p.ldy = ldy;
         p.status = d->status;
-        p.k_splits = gemm_k_splits(M, N, K, d->num_sms);
-        p.n_items *= p.k_splits;
-        if (p.k_splits > 1) {
-            const size_t need = (size_t)p.k_splits * (size_t)M * (size_t)N * sizeof(float);
-            if (!workspace || ws_bytes < need || !aligned16(workspace))
-                return fail(AWQ_ERR_WORKSPACE, "w4a16_gemm: workspace missing or too small "
-                                               "(see w4a16_gemm_workspace_size)");
-            p.ws_partial = static_cast<float*>(workspace);
-        }
+        if (k_splits > 1) p.ws_partial = reinterpret_cast<float*>(ws + xs_bytes);
         e = awq::launch_tc_gemm(map, p, d->num_sms, st);
-        if (e == cudaSuccess && p.k_splits > 1)
-            e = awq::launch_splitk_reduce(p.ws_partial, p.k_splits, M, N, Y, ldy, d->num_sms, st);
+        if (e == cudaSuccess && k_splits > 1)
+            e = awq::launch_splitk_reduce(p.ws_partial, k_splits, M, N, Y, ldy, d->num_sms, st);
     }
     return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+awq_status w4a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx, const uint32_t* qweight,
+                      const uint16_t* scales, const uint16_t* zeros, int64_t N, int group,
+                      uint16_t* Y, int64_t ldy, void* workspace, size_t ws_bytes,
+                      awq_stream_t stream) {
+    return gemm_impl("w4a16_gemm", X, M, K, ldx, nullptr, qweight, scales, zeros, N, group, Y,
+                     ldy, workspace, ws_bytes, stream);
+}
+
+size_t w4a16_gemm_scaled_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0 || K % AWQ_GROUP) return 0;
+    return scaled_x_bytes(M, K) + w4a16_gemm_workspace_size(M, N, K);
+}
+
+awq_status w4a16_gemm_scaled(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
+                             const float* inv_s, const uint32_t* qweight, const uint16_t* scales,
+                             const uint16_t* zeros, int64_t N, int group, uint16_t* Y, int64_t ldy,
+                             void* workspace, size_t ws_bytes, awq_stream_t stream) {
+    if (!inv_s) return fail(AWQ_ERR_INVALID_ARG, "w4a16_gemm_scaled: null inv_s");
+    return gemm_impl("w4a16_gemm_scaled", X, M, K, ldx, inv_s, qweight, scales, zeros, N, group,
+                     Y, ldy, workspace, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -118,6 +118,23 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// x * inv_s for 8 consecutive activations: fp32 product, rounded once to
+// fp32 and once to fp16 (the fused form of the caller's "divide by s").
+__device__ __forceinline__ uint4 scale_x8(uint4 v, const float* inv_s) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(inv_s));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(inv_s) + 1);
+    const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __half2 h = *reinterpret_cast<const __half2*>(&w[j]);
+        const __half2 r = __floats2half2_rn(__fmul_rn(__low2float(h), f[2 * j]),
+                                            __fmul_rn(__high2float(h), f[2 * j + 1]));
+        w[j] = *reinterpret_cast<const uint32_t*>(&r);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // 8 physical activations (x0..x7) -> the B-fragment order of the permuted k:
 // (x0,x4) (x1,x5) (x2,x6) (x3,x7).
 __device__ __forceinline__ uint4 permute_x8(uint4 v) {
@@ -170,7 +187,11 @@ __device__ __forceinline__ void load_group_x(GroupX<NB>& in, const GemvParams& p
         const uint4* xp = reinterpret_cast<const uint4*>(p.X + (int64_t)tok * p.ldx +
                                                          (int64_t)gi * kGroup + 32 * t);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) in.x[nb][i] = permute_x8(__ldg(xp + i));
+        for (int i = 0; i < 4; ++i) {
+            uint4 v = __ldg(xp + i);
+            if (p.inv_s) v = scale_x8(v, p.inv_s + (int64_t)gi * kGroup + 32 * t + 8 * i);
+            in.x[nb][i] = permute_x8(v);
+        }
     }
 }
 
@@ -321,8 +342,9 @@ __global__ void __launch_bounds__(NW * 32, DecCfg<NB>::kMinBlocks)
         for (int cix = threadIdx.x; cix < chunks; cix += kDecThreads) {
             const int m = cix / (p.G * 16), rem = cix - m * p.G * 16;
             const int gl = rem >> 4, k8 = rem & 15;
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+            uint4 v = __ldg(reinterpret_cast<const uint4*>(
                 p.X + (int64_t)m * p.ldx + (int64_t)gl * kGroup + k8 * 8));
+            if (p.inv_s) v = scale_x8(v, p.inv_s + (int64_t)gl * kGroup + k8 * 8);
             const int tt = k8 >> 2, ii = k8 & 3;
             *reinterpret_cast<uint4*>(xsm + m * xrow + gl * 256 + (ii * 4 + tt) * 16) =
                 permute_x8(v);

@@ -48,6 +48,7 @@ struct GemvParams {
     int64_t ldy;
     unsigned* status;
     int early_weights;   // 1: weights may be fetched before the previous kernel completes
+    const float* inv_s;  // [K] or null: X is used as fp16(X * inv_s) (fused input scaling)
 };
 // mapW: 2-D tensor map of qweight as uint32 [N rows][K/8 words], box 48 words x 16 rows.
 cudaError_t launch_gemv(const CUtensorMap& mapW, const GemvParams& p, int num_sms,
@@ -84,6 +85,9 @@ constexpr int kSearchTokensPerItem = 512;
 
 cudaError_t launch_tc_gemm(const CUtensorMap& mapX, const TcParams& p, int num_sms,
                            cudaStream_t st);
+// Xs[m, k] = fp16(fp32(X[m, k]) * inv_s[k]) into a dense [M, K] buffer.
+cudaError_t launch_scale_x(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
+                           const float* inv_s, uint16_t* Xs, int num_sms, cudaStream_t st);
 // Y = fp16(sum over splits of ws_partial), the splits added in order.
 cudaError_t launch_splitk_reduce(const float* ws_partial, int k_splits, int64_t M, int64_t N,
                                  uint16_t* Y, int64_t ldy, int num_sms, cudaStream_t st);

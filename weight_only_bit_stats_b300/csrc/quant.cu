@@ -187,7 +187,41 @@ __global__ void __launch_bounds__(256)
     for (int64_t k = threadIdx.x; k < K / 4; k += blockDim.x) dst[k] = src[k];
 }
 
+// Xs = fp16(fp32(X) * inv_s), 8 activations per thread (K % 8 == 0).
+__global__ void __launch_bounds__(256)
+    scale_x_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K, int64_t ldx,
+                   const float* __restrict__ inv_s, uint16_t* __restrict__ Xs) {
+    const int64_t per_row = K / 8, total = M * per_row;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = i / per_row, k = (i - m * per_row) * 8;
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(X + m * ldx + k));
+        const float4 a = __ldg(reinterpret_cast<const float4*>(inv_s + k));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(inv_s + k) + 1);
+        const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __half2 h = *reinterpret_cast<const __half2*>(&w[j]);
+            const __half2 r = __floats2half2_rn(__fmul_rn(__low2float(h), f[2 * j]),
+                                                __fmul_rn(__high2float(h), f[2 * j + 1]));
+            w[j] = *reinterpret_cast<const uint32_t*>(&r);
+        }
+        *reinterpret_cast<uint4*>(Xs + m * K + k) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_scale_x(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
+                           const float* inv_s, uint16_t* Xs, int num_sms, cudaStream_t st) {
+    const int64_t total = M * (K / 8);
+    if (total == 0) return cudaSuccess;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > (int64_t)num_sms * 16) blocks = (int64_t)num_sms * 16;
+    scale_x_kernel<<<(unsigned)blocks, 256, 0, st>>>(X, M, K, ldx, inv_s, Xs);
+    return cudaGetLastError();
+}
 
 int cand_blocks(int64_t K) { return (int)((K + kCandThreads - 1) / kCandThreads); }
 
