@@ -228,6 +228,15 @@ awq_status awq_set_weight_prefetch(int enable);
  * synchronisation itself failed. */
 awq_status awq_sync_status(awq_stream_t stream);
 
+/* Diagnostic of the failure path (no counterpart on the AWQ pages): every
+ * device-side wait in the library's kernels is bounded, and a wait that runs
+ * out records AWQ_ERR_TIMEOUT in the status word and lets the kernel return,
+ * so the context stays usable.  This call launches one small kernel whose
+ * bounded wait, limited to limit_us microseconds (1 .. 1e6), is on a barrier
+ * that nothing arrives on; awq_sync_status() then returns AWQ_ERR_TIMEOUT
+ * (and clears it).  Nothing faults, traps or hangs. */
+awq_status awq_selftest_wait_timeout(int64_t limit_us, awq_stream_t stream);
+
 /* Static text for the last error returned by a call on this host thread. */
 const char* awq_last_error_string(void);
 

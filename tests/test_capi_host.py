@@ -79,6 +79,8 @@ def test_host_argument_checks(capi):
     # decode weight prefetch: a flag, 0 or 1 only (host-side setting)
     assert capi.awq_set_weight_prefetch(2) == 1
     assert capi.awq_set_weight_prefetch(1) == 0 and capi.awq_set_weight_prefetch(0) == 0
+    # timeout self-test: the limit is checked before any device call
+    assert capi.awq_selftest_wait_timeout(0, None) == 1
     assert capi.awq_last_error_string()
 
 

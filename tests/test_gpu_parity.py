@@ -400,3 +400,17 @@ def test_gemm_scaled_fused_input(wb, orc, M):
     y_plain = host(wb.w4a16_gemm(dev(Xs.view(np.float16)), qw, sc, ze))
     assert np.array_equal(y_fused.view(np.uint16), y_plain.view(np.uint16))
     assert rel_err(y_fused, orc.w4a16_gemm(Xs, rq, rs, rz)) <= GEMM_TOL
+
+
+def test_bounded_wait_timeout_reports_and_recovers(wb, orc):
+    """A device wait that runs out (a barrier nothing arrives on, 2 ms limit)
+    records AWQ_ERR_TIMEOUT, which awq_sync_status reports once and clears;
+    the context stays usable for the next call."""
+    stream = torch.cuda.current_stream().cuda_stream
+    assert wb.lib().awq_selftest_wait_timeout(2000, stream) == 0
+    with pytest.raises(wb.AwqError) as e:
+        wb.sync_status()
+    assert e.value.code == 7
+    wb.sync_status()                       # cleared
+    _pack_check(wb, orc, sg.layer_inputs(18, 0, 64, 256, 0)[0], None)
+    wb.sync_status()

@@ -64,6 +64,7 @@ SIGNATURES = (
                                  _sz, _p]),
     ("w4a16_gemm_scaled_workspace_size", _sz, [_i64, _i64, _i64]),
     ("awq_set_weight_prefetch", _int, [_int]),
+    ("awq_selftest_wait_timeout", _int, [_i64, _p]),
     ("awq_sync_status", _int, [_p]),
     ("awq_last_error_string", ctypes.c_char_p, []),
     ("awq_version", _int, []),

@@ -149,6 +149,17 @@ extern "C" {
 
 int awq_version(void) { return 100; }
 
+awq_status awq_selftest_wait_timeout(int64_t limit_us, awq_stream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000)
+        return fail(AWQ_ERR_INVALID_ARG, "selftest_wait_timeout: limit must be 1 us .. 1 s");
+    DevInfo* d = nullptr;
+    awq_status s = device_info(&d);
+    if (s) return s;
+    cudaError_t e = awq::launch_wait_timeout_selftest((unsigned long long)limit_us * 1000ull,
+                                                      d->status, (cudaStream_t)stream);
+    return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
+}
+
 awq_status awq_set_weight_prefetch(int enable) {
     if (enable != 0 && enable != 1) return fail(AWQ_ERR_INVALID_ARG, "set_weight_prefetch: flag must be 0 or 1");
     g_early_weights.store(enable, std::memory_order_relaxed);

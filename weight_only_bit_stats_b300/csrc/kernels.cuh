@@ -19,6 +19,10 @@ cudaError_t launch_act_stats(const uint16_t* X, int64_t T, int64_t K, int64_t ld
 cudaError_t launch_act_mean(const int64_t* abs_sum, int64_t n_tokens, int64_t K, double* mean,
                             cudaStream_t st);
 
+// Diagnostic: a bounded wait on an mbarrier nothing arrives on (stats.cu).
+cudaError_t launch_wait_timeout_selftest(unsigned long long limit_ns, unsigned* status,
+                                         cudaStream_t st);
+
 // ---- candidate scales, pack, search reduction (quant.cu) ----
 int cand_blocks(int64_t K);
 // ws_r: [n_alpha, K] fp64; ws_mm: [n_alpha, cand_blocks(K), 2] fp64.

@@ -77,7 +77,28 @@ __global__ void act_mean_kernel(const int64_t* __restrict__ abs_sum, int64_t n_t
     if (k < K) mean[k] = ((double)abs_sum[k] / 16777216.0) / (double)n_tokens;
 }
 
+// Diagnostic: one warp waits, with the kernels' bounded wait and a short
+// limit, for phase 0 of an mbarrier that nothing arrives on.  The wait runs
+// out, records the timeout status and the kernel returns.
+__global__ void wait_timeout_selftest_kernel(unsigned long long limit_ns, unsigned* status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    mbar_wait(&bar, 0, &abort, status, limit_ns);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout_selftest(unsigned long long limit_ns, unsigned* status,
+                                         cudaStream_t st) {
+    wait_timeout_selftest_kernel<<<1, 32, 0, st>>>(limit_ns, status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_act_stats(const uint16_t* X, int64_t T, int64_t K, int64_t ldx,
                              unsigned long long* abs_sum, unsigned* status, int num_sms,
