@@ -46,11 +46,11 @@ WORKLOAD = ("LLaMA-7B-shaped decode GEMV, M=1, projections qkv 12288x4096, o 409
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 # DRAM traffic of the fused search kernel, dram__bytes_read.sum +
 # dram__bytes_write.sum summed over the four search launches of one step of
-# this workload in one ncu capture (profiles/tc_search_llama7b_decode_step.md),
+# this workload in one ncu capture (profiles/tc_search_llama7b_qkv.md),
 # valid only while the kernel's sources are the ones captured.
-SEARCH_TRAFFIC = {"bytes_per_step": 105569536 + 2833920 + 38599680 + 0 + 185260544 + 204032 +
-                                    103309568 + 127744,
-                  "src_sha": "34fc5bc68177dde3"}
+SEARCH_TRAFFIC = {"bytes_per_step": 105570560 + 2852352 + 38462976 + 0 + 185350656 + 187648 +
+                                    103267328 + 426496,
+                  "src_sha": "e22f2f85c3ad31cf"}
 SEARCH_SOURCES = ("tc.cu", "common.cuh", "kernels.cuh")
 
 
