@@ -414,3 +414,47 @@ def test_bounded_wait_timeout_reports_and_recovers(wb, orc):
     wb.sync_status()                       # cleared
     _pack_check(wb, orc, sg.layer_inputs(18, 0, 64, 256, 0)[0], None)
     wb.sync_status()
+
+
+@pytest.mark.parametrize("M", [1, 7, 16])
+@pytest.mark.parametrize("N,K", [(2384, 256), (2400, 1152), (4752, 384), (3000, 11008)])
+def test_decode_cross_cta_split(wb, orc, M, N, K):
+    """Just over one to two 16-row slabs per SM (149-297 slabs), with long
+    and short K: every output against the oracle, and repeated calls
+    bit-identical (the split and the order of the additions are fixed)."""
+    y = _gemm_check(wb, orc, N, K, M, seed=1)
+    W, _, X, _ = sg.layer_inputs(13, 1, N, K, 0, M=M)
+    rq, rs, rz = orc.pack_int4(W)
+    args = (dev(X), dev(rq.view(np.int32)), dev(rs.view(np.float16)), dev(rz.view(np.float16)))
+    for _ in range(3):
+        Y = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+        wb.w4a16_gemm(*args, out=Y)
+        assert np.array_equal(host(Y).view(np.uint16), y.view(np.uint16))
+    wb.sync_status()
+
+
+def test_decode_two_streams(wb, orc):
+    """Decodes on two streams at once (programmatic dependent launch and
+    early weight reads stay per stream): each stream's outputs equal its
+    single-stream result bit for bit."""
+    jobs = []
+    for j, (N, K) in enumerate([(4096, 4096), (5120, 2048)]):
+        W, _, X, _ = sg.layer_inputs(16, j, N, K, 0, M=1)
+        qw, sc, ze = wb.pack_int4(dev(W))
+        x = dev(X)
+        ref = host(wb.w4a16_gemm(x, qw, sc, ze))
+        jobs.append((x, qw, sc, ze, ref, N))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    outs = [[], []]
+    for _ in range(20):
+        for (x, qw, sc, ze, ref, N), st, o in zip(jobs, streams, outs):
+            with torch.cuda.stream(st):
+                Y = torch.full((1, N), float("nan"), dtype=torch.float16, device="cuda")
+                wb.w4a16_gemm(x, qw, sc, ze, out=Y, stream=st)
+                o.append(Y)
+    torch.cuda.synchronize()
+    for (x, qw, sc, ze, ref, N), o in zip(jobs, outs):
+        for Y in o:
+            assert np.array_equal(host(Y).view(np.uint16), ref.view(np.uint16))
+    wb.sync_status()
