@@ -71,13 +71,21 @@ template <int MODE>
 __device__ __forceinline__ Item decode_item(int item, const TcParams& p) {
     Item it;
     if (MODE == kModeGemm) {
-        // consecutive CTAs share the weight tile: the token tiles of one
-        // weight tile run together, so its packed words leave DRAM once and
-        // the activations (a few tens of MB) stay in L2
-        it.t_tile = item % p.t_tiles;
-        const int rest = item / p.t_tiles;
-        it.n_tile = rest % p.n_tiles;
-        it.split = rest / p.n_tiles;
+        // token tiles in bands of up to 8 (2048 tokens): within a band,
+        // consecutive CTAs share a weight tile (the band's token tiles of one
+        // weight tile run together) and the weight tiles go round, so the
+        // band's activations stay in L2 while the packed words stream by,
+        // once per band
+        const int per_split = p.t_tiles * p.n_tiles;
+        it.split = item / per_split;
+        const int q = item - it.split * per_split;
+        const int band_tiles = p.t_tiles < 8 ? p.t_tiles : 8;
+        const int band = q / (band_tiles * p.n_tiles);
+        const int rb = q - band * band_tiles * p.n_tiles;
+        const int bt = (band + 1) * band_tiles <= p.t_tiles ? band_tiles
+                                                            : p.t_tiles - band * band_tiles;
+        it.t_tile = band * band_tiles + rb % bt;
+        it.n_tile = rb / bt;
         it.alpha = 0;
         it.g0 = (int)((int64_t)it.split * p.G / p.k_splits);
         it.g1 = (int)((int64_t)(it.split + 1) * p.G / p.k_splits);
@@ -278,6 +286,16 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 z1024, __half2 zne
                       prmt(u2, u3, 0x7632));
 }
 
+// Hint: bring the 128-byte line holding ptr into L2.
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
+// Groups of packed words a producer row requests into L2 ahead of its own
+// loads (which run one group ahead): with ~0.7 us of MMA work per group, six
+// groups cover a DRAM miss several times over.
+constexpr int kProdPrefetch = 6;
+
 __device__ void role_prod_gemm(const TcParams& p, uint8_t* As, SmemCtl* ctl, int r, int lane) {
     volatile int* abort = &ctl->abort;
     const int64_t wstride = p.K / 8;
@@ -296,10 +314,19 @@ __device__ void role_prod_gemm(const TcParams& p, uint8_t* As, SmemCtl* ctl, int
             for (int j = 0; j < 4; ++j) cur[j] = __ldg(qrow + (int64_t)it.g0 * 4 + j);
             csc = __ldg(srow + it.g0);
             cze = __ldg(zrow + it.g0);
+            // the row's scales and zero-points of this item, and its next
+            // groups of packed words
+            for (int g = it.g0; g < it.g1; g += 64) {
+                prefetch_l2(srow + g);
+                prefetch_l2(zrow + g);
+            }
+            for (int g = it.g0 + 2; g < it.g1 && g < it.g0 + kProdPrefetch; ++g)
+                prefetch_l2(qrow + (int64_t)g * 4);
         }
         for (int g = it.g0; g < it.g1; ++g) {
             uint4 nxt[4];
             uint16_t nsc = 0, nze = 0;
+            if (valid && g + kProdPrefetch < it.g1) prefetch_l2(qrow + (int64_t)(g + kProdPrefetch) * 4);
             if (valid && g + 1 < it.g1) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) nxt[j] = __ldg(qrow + (int64_t)(g + 1) * 4 + j);
