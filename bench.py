@@ -48,9 +48,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # dram__bytes_write.sum summed over the four search launches of one step of
 # this workload in one ncu capture (profiles/tc_search_llama7b_qkv.md),
 # valid only while the kernel's sources are the ones captured.
-SEARCH_TRAFFIC = {"bytes_per_step": 105570560 + 2852352 + 38462976 + 0 + 185350656 + 187648 +
-                                    103267328 + 426496,
-                  "src_sha": "e22f2f85c3ad31cf"}
+SEARCH_TRAFFIC = {"bytes_per_step": 105571584 + 2872320 + 38458624 + 0 + 185359104 + 186624 +
+                                    103278080 + 148224,
+                  "src_sha": "09baa005635d0117"}
 SEARCH_SOURCES = ("tc.cu", "common.cuh", "kernels.cuh")
 
 
