@@ -14,8 +14,8 @@ Method source: "AWQ: Activation-aware Weight Quantization for On-Device LLM
 Compression and Acceleration" (fdeinterviews.com/papers/awq), third
 paragraph (scaling trick, s = average activation magnitude ** alpha, alpha
 by grid search on a calibration set, every weight in low bits), seventh
-paragraph (only activation statistics are collected), last paragraph
-(4 bits).  Group size 128, asymmetric fp16 scale/zero, mean |x|, output MSE
+paragraph (only activation statistics are collected), fourth and last
+paragraphs (evaluated at 3 and 4 bits; 4 bits the default).  Group size 128, asymmetric fp16 scale/zero, mean |x|, output MSE
 and the 20-point alpha grid are the workload definition, not the pages'.
 """
 from __future__ import annotations
@@ -63,6 +63,10 @@ def _lib():
         lib.awqo_act_mean.argtypes = [_ptr, _i64, _i64, _ptr]
         lib.awqo_candidate_scales.argtypes = [_ptr, _i64, ctypes.c_double, _ptr]
         lib.awqo_quantize.argtypes = [_ptr, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr]
+        lib.awqo_quantize_bits.argtypes = [_ptr, _i64, _i64, _i64, _ptr, ctypes.c_int, _ptr,
+                                           _ptr, _ptr]
+        lib.awqo_pack_planes3.argtypes = [_ptr, _i64, _i64, _ptr]
+        lib.awqo_unpack_planes3.argtypes = [_ptr, _i64, _i64, _ptr]
         lib.awqo_pack_nibbles.argtypes = [_ptr, _i64, _i64, _ptr]
         lib.awqo_unpack_nibbles.argtypes = [_ptr, _i64, _i64, _ptr]
         lib.awqo_dequant.argtypes = [_ptr, _ptr, _ptr, _i64, _i64, _ptr]
@@ -154,9 +158,11 @@ def candidate_scales(m: np.ndarray, alpha: float) -> np.ndarray:
 
 # ---- steps a3/a5: quantiser and packing ---------------------------------
 
-def quantize(W: np.ndarray, s: np.ndarray | None = None):
-    """INT4 levels of W*diag(s): returns (q uint8 [N,K], scales fp16-bits
-    [N,K/128], zeros fp16-bits [N,K/128])."""
+def quantize(W: np.ndarray, s: np.ndarray | None = None, bits: int = 4):
+    """Levels 0..2^bits - 1 (bits 4, or 3) of W*diag(s): returns (q uint8
+    [N,K], scales fp16-bits [N,K/128], zeros fp16-bits [N,K/128])."""
+    if bits not in (3, 4):
+        raise OracleError("bits must be 3 or 4")
     b = _bits(W)
     N, K = b.shape
     if K % GROUP:
@@ -170,7 +176,7 @@ def quantize(W: np.ndarray, s: np.ndarray | None = None):
         s = np.ascontiguousarray(s, dtype=np.float32)
         assert s.size == K
         sp = _p(s)
-    r = _lib().awqo_quantize(_p(b), N, K, K, sp, _p(q), _p(sc), _p(ze))
+    r = _lib().awqo_quantize_bits(_p(b), N, K, K, sp, bits, _p(q), _p(sc), _p(ze))
     if r:
         raise OracleError(f"quantize: status {r}")
     return q, sc, ze
@@ -192,6 +198,32 @@ def unpack_nibbles(words: np.ndarray, K: int) -> np.ndarray:
     return q
 
 
+def pack_planes3(q: np.ndarray) -> np.ndarray:
+    """3-bit levels -> uint32 [N, K/32 * 3]: per 32 levels, bit plane p in
+    word p (level i of the block at bit i)."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    N, K = q.shape
+    if K % 32:
+        raise OracleError("K must be a multiple of 32")
+    w = np.empty((N, K // 32 * 3), dtype=np.uint32)
+    _lib().awqo_pack_planes3(_p(q), N, K, _p(w))
+    return w
+
+
+def unpack_planes3(words: np.ndarray, K: int) -> np.ndarray:
+    w = np.ascontiguousarray(words, dtype=np.uint32)
+    N = w.shape[0]
+    q = np.empty((N, K), dtype=np.uint8)
+    _lib().awqo_unpack_planes3(_p(w), N, K, _p(q))
+    return q
+
+
+def pack_int3(W: np.ndarray, s: np.ndarray | None = None):
+    """(bit planes uint32 [N, 3K/32], scales, zeros) of W*diag(s) at 3 bits."""
+    q, sc, ze = quantize(W, s, bits=3)
+    return pack_planes3(q), sc, ze
+
+
 def pack_int4(W: np.ndarray, s: np.ndarray | None = None):
     """(qweight uint32 [N,K/8], scales, zeros) of W*diag(s)."""
     q, sc, ze = quantize(W, s)
@@ -210,11 +242,12 @@ def dequant(q: np.ndarray, scales: np.ndarray, zeros: np.ndarray) -> np.ndarray:
 
 # ---- steps a3/a4: the alpha search ---------------------------------------
 
-def search_residual(W: np.ndarray, s: np.ndarray | None, quant=None) -> np.ndarray:
+def search_residual(W: np.ndarray, s: np.ndarray | None, quant=None,
+                    bits: int = 4) -> np.ndarray:
     """E = Q(W diag(s)) diag(s)^-1 - W in fp64, [N,K]."""
     b = _bits(W)
     N, K = b.shape
-    q, sc, ze = quant if quant is not None else quantize(b, s)
+    q, sc, ze = quant if quant is not None else quantize(b, s, bits)
     sp = None
     if s is not None:
         s = np.ascontiguousarray(s, dtype=np.float32)
@@ -226,7 +259,7 @@ def search_residual(W: np.ndarray, s: np.ndarray | None, quant=None) -> np.ndarr
 
 
 def search_mse(W: np.ndarray, X: np.ndarray, s: np.ndarray | None,
-               row_chunk: int = 4096) -> float:
+               row_chunk: int = 4096, bits: int = 4) -> float:
     """Output MSE of Q(W diag(s)) diag(s)^-1 against W on activations X:
     ||X E^T||_F^2 / (T N), all in fp64 (numpy matmul as the library step)."""
     b = _bits(W)
@@ -237,14 +270,14 @@ def search_mse(W: np.ndarray, X: np.ndarray, s: np.ndarray | None,
         s = np.ascontiguousarray(s, dtype=np.float32)
     total = 0.0
     for n0 in range(0, N, row_chunk):
-        E = search_residual(b[n0:n0 + row_chunk], s)
+        E = search_residual(b[n0:n0 + row_chunk], s, bits=bits)
         Y = X64 @ E.T
         total += float(np.sum(Y * Y))
     return total / (T * N)
 
 
 def search_scale(W: np.ndarray, X: np.ndarray, m: np.ndarray,
-                 alphas=ALPHA_GRID):
+                 alphas=ALPHA_GRID, bits: int = 4):
     """Grid search over alpha: returns (s_best fp32 [K], mse fp64 [n_alpha],
     best index).  Ties go to the lowest index (ascending scan, strict <)."""
     mse = np.empty(len(alphas), dtype=np.float64)
@@ -252,7 +285,7 @@ def search_scale(W: np.ndarray, X: np.ndarray, m: np.ndarray,
     for i, a in enumerate(alphas):
         s = candidate_scales(m, a)
         cands.append(s)
-        mse[i] = search_mse(W, X, s)
+        mse[i] = search_mse(W, X, s, bits=bits)
     best = 0
     for i in range(1, len(alphas)):
         if mse[i] < mse[best]:

@@ -12,11 +12,14 @@
  *     average activation magnitude raised to a power alpha; alpha comes from a
  *     quick grid search on a small calibration set; every weight stays in low
  *     bits.  Seventh paragraph: only activation statistics are collected.
- *     Last paragraph: 4 bits is the default.
- *   - Group size 128, asymmetric levels 0..15 with an fp16 scale and fp16
- *     zero-point per group, 8 nibbles per uint32, mean |x| as the average
- *     magnitude, output MSE as the search objective and the 20-point alpha
- *     grid are not on the pages; they are the stated workload definition.
+ *     Fourth paragraph: the method was evaluated at 3 and 4 bits; last
+ *     paragraph: 4 bits is the default, 3 bits possible with a noticeable
+ *     gap.
+ *   - Group size 128, asymmetric levels 0..15 (0..7 at 3 bits) with an fp16
+ *     scale and fp16 zero-point per group, 8 nibbles per uint32 (3 bit
+ *     planes per 32 levels at 3 bits), mean |x| as the average magnitude,
+ *     output MSE as the search objective and the 20-point alpha grid are
+ *     not on the pages; they are the stated workload definition.
  *
  * Every value the method rounds is rounded at exactly one stated point:
  * "fp32(expr)" means expr is evaluated exactly or in fp64 and then rounded
@@ -118,17 +121,19 @@ void awqo_candidate_scales(const double* m, int64_t K, double alpha, float* s) {
 
 /* ---- steps a3/a5: quantise one row-group of 128 weights --------------- */
 
-/* Asymmetric round-to-nearest INT4 of w' = W*s over one group:
+/* Asymmetric round-to-nearest of w' = W*s over one group, with levels
+ * 0..qmax (qmax = 2^bits - 1: 15 at 4 bits, 7 at 3 bits):
  *   1. w'_k   = fp32(W_k * s_k)                   (s_k = 1 when s is NULL)
  *   2. lo, hi = min, max of w'
- *   3. d      = fp32(fp32(hi - lo) / 15)
+ *   3. d      = fp32(fp32(hi - lo) / qmax)
  *   4. scale  = fp16_rn(max(d, 2^-14))            (stored)
- *   5. z      = clamp(rint(fp32(-lo / scale)), 0, 15)   (stored as fp16)
- *   6. q_k    = clamp(rint(fp32(w'_k / scale)) + z, 0, 15)
+ *   5. z      = clamp(rint(fp32(-lo / scale)), 0, qmax)   (stored as fp16)
+ *   6. q_k    = clamp(rint(fp32(w'_k / scale)) + z, 0, qmax)
  * rint is round-half-to-even.  Returns OR_ERR_NONFINITE if an input is not
  * finite or the scale overflows fp16. */
-static int quant_group(const uint16_t* w, const float* s, uint8_t* q,
+static int quant_group(const uint16_t* w, const float* s, int qmax, uint8_t* q,
                        uint16_t* scale_out, uint16_t* zero_out) {
+    const float fq = (float)qmax;
     float wp[GROUP];
     for (int k = 0; k < GROUP; ++k) {
         double wk = awqo_h2d(w[k]);
@@ -143,21 +148,21 @@ static int quant_group(const uint16_t* w, const float* s, uint8_t* q,
         if (wp[k] > hi) hi = wp[k];
     }
     float range = (float)((double)hi - (double)lo);
-    float d = (float)((double)range / 15.0);
+    float d = (float)((double)range / (double)qmax);
     if (d < 0x1p-14f) d = 0x1p-14f;
     uint16_t sh = awqo_d2h_rn((double)d);
     if ((sh & 0x7C00) == 0x7C00) return OR_ERR_NONFINITE;
     double scale = awqo_h2d(sh);
-    /* the zero-point is an integer level 0..15; the clamp maps -0 (from
+    /* the zero-point is an integer level 0..qmax; the clamp maps -0 (from
      * rint of a negative quotient above -0.5) to the integer 0, i.e. +0.0 */
     float zf = rintf((float)(-(double)lo / scale));
     if (!(zf > 0.0f)) zf = 0.0f;
-    if (zf > 15.0f) zf = 15.0f;
+    if (zf > fq) zf = fq;
     for (int k = 0; k < GROUP; ++k) {
         float t = (float)((double)wp[k] / scale);
         float v = rintf(t) + zf;                     /* exact: |rint(t)| < 2^24 or clamped */
         if (v < 0.0f) v = 0.0f;
-        if (v > 15.0f) v = 15.0f;
+        if (v > fq) v = fq;
         q[k] = (uint8_t)v;
     }
     *scale_out = sh;
@@ -166,22 +171,30 @@ static int quant_group(const uint16_t* w, const float* s, uint8_t* q,
 }
 
 /* Quantise W [N,K] (row stride ldw) with per-input-channel scales s [K]
- * (NULL: plain round-to-nearest).  q: [N,K] one level per byte;
- * scales, zeros: [N, K/128] fp16. */
-int awqo_quantize(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
-                  const float* s, uint8_t* q, uint16_t* scales, uint16_t* zeros) {
-    if (N < 0 || K < 0 || K % GROUP || ldw < K) return OR_ERR_ARG;
+ * (NULL: plain round-to-nearest) to `bits` bits (3 or 4).  q: [N,K] one
+ * level per byte; scales, zeros: [N, K/128] fp16. */
+int awqo_quantize_bits(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                       const float* s, int bits, uint8_t* q, uint16_t* scales,
+                       uint16_t* zeros) {
+    if (N < 0 || K < 0 || K % GROUP || ldw < K || (bits != 3 && bits != 4)) return OR_ERR_ARG;
+    const int qmax = (1 << bits) - 1;
     int64_t G = K / GROUP;
     int bad = 0;
     /* rows are independent; the threads only split the row range */
     #pragma omp parallel for schedule(static) reduction(|:bad)
     for (int64_t n = 0; n < N; ++n)
         for (int64_t g = 0; g < G; ++g) {
-            int r = quant_group(W + n * ldw + g * GROUP, s ? s + g * GROUP : NULL,
+            int r = quant_group(W + n * ldw + g * GROUP, s ? s + g * GROUP : NULL, qmax,
                                 q + n * K + g * GROUP, scales + n * G + g, zeros + n * G + g);
             if (r) bad |= r;
         }
     return bad;
+}
+
+/* The 4-bit quantiser of steps a3/a5. */
+int awqo_quantize(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                  const float* s, uint8_t* q, uint16_t* scales, uint16_t* zeros) {
+    return awqo_quantize_bits(W, N, K, ldw, s, 4, q, scales, zeros);
 }
 
 /* ---- packing: 8 nibbles per uint32 --------------------------------------- */
@@ -202,6 +215,33 @@ void awqo_unpack_nibbles(const uint32_t* words, int64_t N, int64_t K, uint8_t* q
     for (int64_t n = 0; n < N; ++n)
         for (int64_t k = 0; k < K; ++k)
             q[n * K + k] = (uint8_t)((words[n * W8 + k / 8] >> (4 * (k % 8))) & 15);
+}
+
+/* ---- 3-bit packing: three bit planes per 32 levels ----------------------
+ * Levels k = 32 j .. 32 j + 31 of row n occupy words 3 j, 3 j + 1, 3 j + 2 of
+ * that row; word 3 j + p holds bit p of level 32 j + i at bit i.  Exactly 3
+ * bits per weight, and a group of 128 levels is 12 whole words. */
+void awqo_pack_planes3(const uint8_t* q, int64_t N, int64_t K, uint32_t* words) {
+    int64_t B = K / 32;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t j = 0; j < B; ++j)
+            for (int p = 0; p < 3; ++p) {
+                uint32_t w = 0;
+                for (int i = 0; i < 32; ++i)
+                    w |= (uint32_t)((q[n * K + 32 * j + i] >> p) & 1) << i;
+                words[(n * B + j) * 3 + p] = w;
+            }
+}
+
+void awqo_unpack_planes3(const uint32_t* words, int64_t N, int64_t K, uint8_t* q) {
+    int64_t B = K / 32;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) {
+            const uint32_t* w = words + (n * B + k / 32) * 3;
+            int i = (int)(k % 32);
+            q[n * K + k] = (uint8_t)(((w[0] >> i) & 1) | (((w[1] >> i) & 1) << 1) |
+                                     (((w[2] >> i) & 1) << 2));
+        }
 }
 
 /* Dequantised weights in fp64: deq[n,k] = (q - z) * scale. */

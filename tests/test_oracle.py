@@ -171,16 +171,18 @@ def _wprime(W16, s):
     return w if s is None else (w * s.astype(np.float32)).astype(np.float32)
 
 
-def _check_nearest(oracle_mod, W16, s):
-    q, sc, ze = oracle_mod.quantize(W16, s)
+def _check_nearest(oracle_mod, W16, s, bits=4):
+    qmax = (1 << bits) - 1
+    q, sc, ze = oracle_mod.quantize(W16, s, bits)
     N, K = W16.shape
     G = K // 128
     wp = _wprime(W16, s).astype(np.float64)
     scale = np.repeat(sc.view(np.float16).astype(np.float64), 128, axis=1)
     z = np.repeat(ze.view(np.float16).astype(np.float64), 128, axis=1)
-    assert np.all(z == np.round(z)) and np.all((z >= 0) & (z <= 15))
-    # brute force: distance to each of the 16 levels
-    levels = (np.arange(16)[None, None, :] - z[..., None]) * scale[..., None]
+    assert np.all(z == np.round(z)) and np.all((z >= 0) & (z <= qmax))
+    assert int(q.max()) <= qmax
+    # brute force: distance to each of the 2^bits levels
+    levels = (np.arange(qmax + 1)[None, None, :] - z[..., None]) * scale[..., None]
     dist = np.abs(levels - wp[..., None])
     best = dist.min(axis=2)
     mine = np.take_along_axis(dist, q[..., None].astype(np.int64), axis=2)[..., 0]
@@ -195,7 +197,7 @@ def _check_nearest(oracle_mod, W16, s):
     deq = (q.astype(np.float64) - z) * scale
     err = np.abs(deq - wp)
     t = np.rint(wp / scale) + z
-    unclamped = (t >= 0) & (t <= 15)
+    unclamped = (t >= 0) & (t <= qmax)
     assert np.all(err[unclamped] <= scale[unclamped] / 2 * (1 + 2.0 ** -20))
     assert np.all(err[~unclamped] <= scale[~unclamped] * (1 + 2.0 ** -10))
     return q, sc, ze
@@ -238,15 +240,16 @@ def test_quantizer_nonfinite_rejected(oracle_mod):
         oracle_mod.quantize(W)
 
 
-def _grid_aligned(rng, N, K):
-    """Weights that lie exactly on a 16-level grid spanning levels 0..15, with
-    power-of-two scales and per-channel power-of-two s: the quantiser must
-    return exactly that grid."""
+def _grid_aligned(rng, N, K, bits=4):
+    """Weights that lie exactly on a 2^bits-level grid spanning levels
+    0..2^bits - 1, with power-of-two scales and per-channel power-of-two s:
+    the quantiser must return exactly that grid."""
+    qmax = (1 << bits) - 1
     G = K // 128
-    q = rng.integers(0, 16, (N, K))
+    q = rng.integers(0, qmax + 1, (N, K))
     q[:, ::128] = 0
-    q[:, 1::128] = 15
-    z = rng.integers(0, 16, (N, G))
+    q[:, 1::128] = qmax
+    z = rng.integers(0, qmax + 1, (N, G))
     scale = np.exp2(rng.integers(-9, -4, (N, G))).astype(np.float64)
     s = np.exp2(rng.integers(-2, 3, K)).astype(np.float32)
     wp = (q - np.repeat(z, 128, axis=1)) * np.repeat(scale, 128, axis=1)
@@ -452,3 +455,92 @@ def test_scale_activations_independent_route(oracle_mod):
     with np.errstate(over="ignore"):
         ref = (X.astype(np.float32) * inv[None, :]).astype(np.float16).view(np.uint16)
     assert np.array_equal(got, ref)
+
+
+# ------------------------------------------------------- 3-bit variant ----
+# The pages evaluate the method at 3 and 4 bits (fourth paragraph) and call
+# 3 bits possible with a noticeable gap (last paragraph).  The 3-bit
+# quantiser is the 4-bit one with levels 0..7; these pins hold it to the
+# same facts.
+
+def test_int3_nearest_level_bruteforce(oracle_mod):
+    W, _, _, _ = sg.layer_inputs(0, 3, 64, 512, 0)
+    _check_nearest(oracle_mod, W, None, bits=3)
+    s = np.exp(_rng(17).uniform(-1.5, 1.5, 512)).astype(np.float32)
+    _check_nearest(oracle_mod, W, s, bits=3)
+
+
+def test_int3_grid_aligned_exact(oracle_mod):
+    W, s, q0, z0, scale0 = _grid_aligned(_rng(18), 16, 512, bits=3)
+    q, sc, ze = oracle_mod.quantize(W, s, bits=3)
+    assert np.array_equal(q, q0)
+    assert np.array_equal(ze.view(np.float16).astype(np.float64), z0)
+    assert np.array_equal(sc.view(np.float16).astype(np.float64), scale0)
+
+
+def test_int3_alpha_zero_is_plain_rtn(oracle_mod):
+    W, X, _, _ = sg.layer_inputs(1, 2, 32, 256, 64)
+    m = oracle_mod.act_mean(oracle_mod.act_stats(X), 64)
+    a = oracle_mod.quantize(W, oracle_mod.candidate_scales(m, 0.0), bits=3)
+    b = oracle_mod.quantize(W, None, bits=3)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+def test_int3_step_is_range_over_seven(oracle_mod):
+    """One group spanning [-1, 6] in steps of 1: scale 1, zero-point 1, and
+    the levels are the values plus one (range / 7 = 1 exactly)."""
+    w = np.tile(np.arange(-1, 7, dtype=np.float64), 16)[None, :].astype(np.float16)
+    q, sc, ze = oracle_mod.quantize(w, None, bits=3)
+    assert sc.view(np.float16)[0, 0] == 1.0 and ze.view(np.float16)[0, 0] == 1.0
+    assert np.array_equal(q[0], (w[0].astype(np.float64) + 1).astype(np.uint8))
+
+
+def test_planes3_layout_golden(oracle_mod):
+    """The 3-bit bit-plane fixture: per 32 levels, word p holds bit p of
+    level i at bit i."""
+    cases = []
+    with open(os.path.join(GOLDEN, "planes3_layout.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            lhs, rhs = line.split("->")
+            cases.append(([(int(k), int(v)) for k, v in (t.split(":") for t in lhs.split())],
+                          [int(h, 16) for h in rhs.split()]))
+    assert len(cases) >= 5
+    for pairs, words in cases:
+        q = np.zeros((1, 32), dtype=np.uint8)
+        for k, v in pairs:
+            q[0, k] = v
+        got = oracle_mod.pack_planes3(q)
+        assert [int(x) for x in got[0]] == words
+        assert np.array_equal(oracle_mod.unpack_planes3(got, 32), q)
+
+
+def test_planes3_roundtrip(oracle_mod):
+    q = _rng(19).integers(0, 8, (5, 384)).astype(np.uint8)
+    w = oracle_mod.pack_planes3(q)
+    assert w.shape == (5, 384 // 32 * 3)            # exactly 3 bits per level
+    assert np.array_equal(oracle_mod.unpack_planes3(w, 384), q)
+
+
+def test_int3_search_mse_bruteforce_exact_tiny(oracle_mod):
+    """N=2, K=128, T=4 at 3 bits: exact rational MSE by enumeration."""
+    W, X, _, _ = sg.layer_inputs(4, 1, 2, 128, 4)
+    s = np.exp(_rng(20).uniform(-1, 1, 128)).astype(np.float32)
+    q, sc, ze = oracle_mod.quantize(W, s, bits=3)
+    assert int(q.max()) <= 7
+    Wv = [[Fraction(float(v)) for v in row] for row in W.astype(np.float64)]
+    Xv = [[Fraction(float(v)) for v in row] for row in X.astype(np.float64)]
+    sv = [Fraction(float(v)) for v in s.astype(np.float64)]
+    scale = [Fraction(float(v)) for v in sc.view(np.float16).astype(np.float64)[:, 0]]
+    zero = [Fraction(float(v)) for v in ze.view(np.float16).astype(np.float64)[:, 0]]
+    total = Fraction(0)
+    for t in range(4):
+        for n in range(2):
+            yq = sum((int(q[n, k]) - zero[n]) * scale[n] * Xv[t][k] / sv[k] for k in range(128))
+            yf = sum(Wv[n][k] * Xv[t][k] for k in range(128))
+            total += (yq - yf) ** 2
+    exact = float(total / 8)
+    assert abs(oracle_mod.search_mse(W, X, s, bits=3) - exact) <= 1e-13 * exact
