@@ -3,6 +3,7 @@
 // library allocates no device memory; every scratch buffer comes from the
 // caller's workspace.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <atomic>
 #include <mutex>
@@ -20,6 +21,16 @@ std::atomic<int> g_early_weights{0};
 __device__ unsigned int g_awq_status;
 
 thread_local const char* g_last_error = "no error";
+
+// An NVTX range named after the C-ABI call it spans, so a profiler's
+// timeline shows each call around its kernels.  Without a profiler attached
+// the push and pop return at once.
+struct CallRange {
+    explicit CallRange(const char* name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange&) = delete;
+    CallRange& operator=(const CallRange&) = delete;
+};
 
 constexpr int kMaxDevices = 64;
 struct DevInfo {
@@ -150,6 +161,7 @@ extern "C" {
 int awq_version(void) { return 100; }
 
 awq_status awq_selftest_wait_timeout(int64_t limit_us, awq_stream_t stream) {
+    const CallRange range("awq_selftest_wait_timeout");
     if (limit_us < 1 || limit_us > 1000000)
         return fail(AWQ_ERR_INVALID_ARG, "selftest_wait_timeout: limit must be 1 us .. 1 s");
     DevInfo* d = nullptr;
@@ -169,6 +181,7 @@ awq_status awq_set_weight_prefetch(int enable) {
 const char* awq_last_error_string(void) { return g_last_error; }
 
 awq_status awq_sync_status(awq_stream_t stream) {
+    const CallRange range("awq_sync_status");
     DevInfo* d = nullptr;
     awq_status s = device_info(&d);
     if (s) return s;
@@ -189,6 +202,7 @@ awq_status awq_sync_status(awq_stream_t stream) {
 
 awq_status awq_act_stats(const uint16_t* X, int64_t T, int64_t K, int64_t ldx, int accumulate,
                          int64_t* abs_sum_q24, awq_stream_t stream) {
+    const CallRange range("awq_act_stats");
     if (T < 0 || K < 0 || (accumulate != 0 && accumulate != 1))
         return fail(AWQ_ERR_INVALID_ARG, "act_stats: negative size or bad accumulate flag");
     if (!abs_sum_q24 || (T > 0 && !X)) return fail(AWQ_ERR_INVALID_ARG, "act_stats: null pointer");
@@ -209,6 +223,7 @@ awq_status awq_act_stats(const uint16_t* X, int64_t T, int64_t K, int64_t ldx, i
 
 awq_status awq_act_mean(const int64_t* abs_sum_q24, int64_t n_tokens, int64_t K, double* mean_abs,
                         awq_stream_t stream) {
+    const CallRange range("awq_act_mean");
     if (n_tokens <= 0 || K < 0) return fail(AWQ_ERR_INVALID_ARG, "act_mean: n_tokens must be > 0");
     if (K > 0 && (!abs_sum_q24 || !mean_abs)) return fail(AWQ_ERR_INVALID_ARG, "act_mean: null pointer");
     DevInfo* d = nullptr;
@@ -226,6 +241,7 @@ size_t awq_candidate_scales_workspace_size(int64_t K, int n_alpha) {
 awq_status awq_candidate_scales(const double* mean_abs, int64_t K, const double* alphas, int n_alpha,
                                 float* s_alpha, void* workspace, size_t ws_bytes,
                                 awq_stream_t stream) {
+    const CallRange range("awq_candidate_scales");
     if (K <= 0 || n_alpha < 1 || n_alpha > AWQ_MAX_ALPHAS)
         return fail(AWQ_ERR_INVALID_ARG, "candidate_scales: bad K or n_alpha");
     if (!mean_abs || !alphas || !s_alpha) return fail(AWQ_ERR_INVALID_ARG, "candidate_scales: null pointer");
@@ -255,6 +271,7 @@ awq_status awq_search_scale(const uint16_t* W, int64_t N, int64_t K, int64_t ldw
                             const double* alphas, int n_alpha, int group, float* s_out,
                             double* mse_out, int32_t* best_idx, float* s_alpha_out,
                             void* workspace, size_t ws_bytes, awq_stream_t stream) {
+    const CallRange range("awq_search_scale");
     if (N <= 0 || K <= 0 || T <= 0 || n_alpha < 1 || n_alpha > AWQ_MAX_ALPHAS)
         return fail(AWQ_ERR_INVALID_ARG, "search_scale: sizes must be positive, 1 <= n_alpha <= 64");
     if (!W || !Xcal || !mean_abs || !alphas || !s_out || !best_idx)
@@ -314,6 +331,7 @@ awq_status awq_search_scale(const uint16_t* W, int64_t N, int64_t K, int64_t ldw
 awq_status awq_pack_int4(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, const float* s,
                          int group, uint32_t* qweight, uint16_t* scales, uint16_t* zeros,
                          awq_stream_t stream) {
+    const CallRange range("awq_pack_int4");
     if (N < 0 || K < 0) return fail(AWQ_ERR_INVALID_ARG, "pack_int4: negative size");
     if ((N > 0 && K > 0) && (!W || !qweight || !scales || !zeros))
         return fail(AWQ_ERR_INVALID_ARG, "pack_int4: null pointer");
@@ -470,6 +488,7 @@ awq_status w4a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx, cons
                       const uint16_t* scales, const uint16_t* zeros, int64_t N, int group,
                       uint16_t* Y, int64_t ldy, void* workspace, size_t ws_bytes,
                       awq_stream_t stream) {
+    const CallRange range("w4a16_gemm");
     return gemm_impl("w4a16_gemm", X, M, K, ldx, nullptr, qweight, scales, zeros, N, group, Y,
                      ldy, workspace, ws_bytes, stream);
 }
@@ -483,6 +502,7 @@ awq_status w4a16_gemm_scaled(const uint16_t* X, int64_t M, int64_t K, int64_t ld
                              const float* inv_s, const uint32_t* qweight, const uint16_t* scales,
                              const uint16_t* zeros, int64_t N, int group, uint16_t* Y, int64_t ldy,
                              void* workspace, size_t ws_bytes, awq_stream_t stream) {
+    const CallRange range("w4a16_gemm_scaled");
     if (!inv_s) return fail(AWQ_ERR_INVALID_ARG, "w4a16_gemm_scaled: null inv_s");
     return gemm_impl("w4a16_gemm_scaled", X, M, K, ldx, inv_s, qweight, scales, zeros, N, group,
                      Y, ldy, workspace, ws_bytes, stream);
