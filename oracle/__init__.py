@@ -276,6 +276,32 @@ def search_mse(W: np.ndarray, X: np.ndarray, s: np.ndarray | None,
     return total / (T * N)
 
 
+def gram(X: np.ndarray) -> np.ndarray:
+    """G = X^T X in fp64 [K,K] from the exact fp64 values of the fp16 X
+    (numpy matmul as the library step)."""
+    X64 = h2d(X)
+    return X64.T @ X64
+
+
+def search_mse_gram(W: np.ndarray, G: np.ndarray, T: int, s: np.ndarray | None,
+                    row_chunk: int = 4096, bits: int = 4) -> float:
+    """The search objective through the Gram matrix G = X^T X of the T
+    calibration tokens: ||X E^T||_F^2 = tr(E G E^T), so the MSE is
+    sum((E G) * E) / (T N), in fp64.  Equal to ``search_mse`` up to fp64
+    rounding; its cost does not grow with T once G exists."""
+    b = _bits(W)
+    N, K = b.shape
+    G = np.ascontiguousarray(G, dtype=np.float64)
+    assert G.shape == (K, K)
+    if s is not None:
+        s = np.ascontiguousarray(s, dtype=np.float32)
+    total = 0.0
+    for n0 in range(0, N, row_chunk):
+        E = search_residual(b[n0:n0 + row_chunk], s, bits=bits)
+        total += float(np.sum((E @ G) * E))
+    return total / (T * N)
+
+
 def search_scale(W: np.ndarray, X: np.ndarray, m: np.ndarray,
                  alphas=ALPHA_GRID, bits: int = 4):
     """Grid search over alpha: returns (s_best fp32 [K], mse fp64 [n_alpha],

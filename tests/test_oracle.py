@@ -544,3 +544,36 @@ def test_int3_search_mse_bruteforce_exact_tiny(oracle_mod):
             total += (yq - yf) ** 2
     exact = float(total / 8)
     assert abs(oracle_mod.search_mse(W, X, s, bits=3) - exact) <= 1e-13 * exact
+
+
+# ------------------------------------------------- Gram-matrix search -----
+# NEXT row f2: the same objective through G = X^T X, which costs 2 N K^2 per
+# alpha instead of 2 T N K (smaller once T > K).
+
+def test_gram_route_equals_output_mse(oracle_mod):
+    """||X E^T||_F^2 = tr(E X^T X E^T): the Gram route gives the direct
+    output MSE to fp64 rounding, for every alpha and at 3 and 4 bits."""
+    W, X, _, _ = sg.layer_inputs(5, 0, 24, 256, 300)
+    m = oracle_mod.act_mean(oracle_mod.act_stats(X), 300)
+    G = oracle_mod.gram(X)
+    assert np.array_equal(G, G.T)
+    for bits in (4, 3):
+        for a in (0.0, 0.35, 0.95):
+            s = oracle_mod.candidate_scales(m, a)
+            d = oracle_mod.search_mse(W, X, s, bits=bits)
+            g = oracle_mod.search_mse_gram(W, G, 300, s, bits=bits)
+            assert abs(g - d) <= 1e-11 * d
+
+
+def test_gram_route_exact_tiny(oracle_mod):
+    """N=2, K=128, T=3: the Gram route against exact rationals."""
+    W, X, _, _ = sg.layer_inputs(5, 1, 2, 128, 3)
+    s = np.exp(_rng(21).uniform(-1, 1, 128)).astype(np.float32)
+    E = oracle_mod.search_residual(W, s)
+    Xv = [[Fraction(float(v)) for v in row] for row in X.astype(np.float64)]
+    Ev = [[Fraction(float(v)) for v in row] for row in E]
+    Gv = [[sum(Xv[t][i] * Xv[t][j] for t in range(3)) for j in range(128)] for i in range(128)]
+    total = sum(Ev[n][i] * Gv[i][j] * Ev[n][j] for n in range(2) for i in range(128) for j in range(128))
+    exact = float(total / 6)
+    g = oracle_mod.search_mse_gram(W, oracle_mod.gram(X), 3, s)
+    assert abs(g - exact) <= 1e-12 * exact
