@@ -164,6 +164,23 @@ awq_status awq_pack_int4(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
                          const float* s, int group, uint32_t* qweight, uint16_t* scales,
                          uint16_t* zeros, awq_stream_t stream);
 
+/* ---- step: 3-bit packing ---------------------------------------------------
+ * The pages evaluate the method at 3 and 4 bits (fourth paragraph; last
+ * paragraph: 3 bits possible, with a noticeable gap).  The quantiser of
+ * awq_pack_int4 with levels 0..7:
+ *   scale = fp16_rn(max(fp32(fp32(hi - lo) / 7), 2^-14))
+ *   z     = clamp(rint(fp32(-lo / scale)), 0, 7)
+ *   q_k   = clamp(rint(fp32(w'_k / scale)) + z, 0, 7)
+ *   planes   [N, 3K/32] uint32: levels 32 j .. 32 j + 31 of a row sit in
+ *            words 3 j .. 3 j + 2 of that row; word 3 j + p holds bit p of
+ *            level 32 j + i at bit i (exactly 3 bits per weight).
+ *   scales   [N, K/128] fp16.     zeros [N, K/128] fp16 holding 0..7.
+ * K % 128 == 0; W and s 16-byte aligned, planes 4-byte, scales/zeros 2-byte.
+ * No matmul consumes this format yet. */
+awq_status awq_pack_int3(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                         const float* s, int group, uint32_t* planes, uint16_t* scales,
+                         uint16_t* zeros, awq_stream_t stream);
+
 /* ---- step: dequantise-fused matmul -----------------------------------------
  * Y = X deq(Wq)^T, deq = (q - z) * scale, fp32 accumulation, fp16 out
  * (pages: fused 4-bit kernels; on-the-fly dequantisation; memory-bound

@@ -143,6 +143,49 @@ def test_pack_nonfinite_flag(wb):
     assert e.value.code == 8
 
 
+# ------------------------------------------------- f3: 3-bit pack -------
+
+def _pack3_check(wb, orc, W, s):
+    pl, sc, ze = wb.pack_int3(dev(W), dev(s) if s is not None else None)
+    rp, rs, rz = orc.pack_int3(W, s)
+    assert np.array_equal(u32(pl), rp)
+    assert np.array_equal(u16(sc), rs)
+    assert np.array_equal(u16(ze), rz)
+
+
+@pytest.mark.parametrize("N,K", [(8, 128), (136, 384), (1024, 1024), (200, 4096)])
+def test_pack_int3_bit_exact(wb, orc, N, K):
+    """The 3-bit pack (levels 0..7, three bit planes per 32 levels) against
+    the oracle, bit for bit, without scales, with random and with AWQ
+    candidate scales."""
+    W, X, _, _ = sg.layer_inputs(10, 3, N, K, 64)
+    _pack3_check(wb, orc, W, None)
+    s_rand = np.exp(np.random.default_rng(N + K + 1).uniform(-2, 2, K)).astype(np.float32)
+    _pack3_check(wb, orc, W, s_rand)
+    m = orc.act_mean(orc.act_stats(X), 64)
+    _pack3_check(wb, orc, W, orc.candidate_scales(m, 0.5))
+    wb.sync_status()
+
+
+def test_pack_int3_edge_groups(wb, orc):
+    K = 256
+    rows = [np.zeros(K), np.full(K, 0.25), np.full(K, -3.0), np.linspace(-1e-6, 1e-6, K),
+            np.linspace(-6e4, 6e4, K), np.r_[np.zeros(K - 1), 5.0], np.linspace(0.5, 2.0, K),
+            np.linspace(-2.0, -0.5, K)]
+    _pack3_check(wb, orc, np.stack(rows).astype(np.float16), None)
+    # exact half-integer quotients: levels at multiples of scale / 2
+    q = np.random.default_rng(4).integers(0, 15, (8, K)) * 0.5
+    q[:, ::128] = 0
+    q[:, 1::128] = 7
+    _pack3_check(wb, orc, (q * 2.0 ** -6).astype(np.float16), None)
+    W = np.zeros((8, 128), dtype=np.float16)
+    W[5, 77] = np.inf
+    wb.pack_int3(dev(W))
+    with pytest.raises(wb.AwqError) as e:
+        wb.sync_status()
+    assert e.value.code == 8
+
+
 # ---------------------------------------------------------- a2-a4 search --
 
 def _search_check(wb, orc, W, X, alphas=None):

@@ -21,7 +21,8 @@ import os
 import torch
 
 __all__ = ["AwqError", "lib", "act_stats", "act_mean", "candidate_scales", "search_scale",
-           "pack_int4", "w4a16_gemm", "w4a16_gemm_scaled", "set_weight_prefetch", "sync_status",
+           "pack_int4", "pack_int3", "w4a16_gemm", "w4a16_gemm_scaled", "set_weight_prefetch",
+           "sync_status",
            "ALPHA_GRID",
            "GROUP"]
 
@@ -58,6 +59,7 @@ SIGNATURES = (
     ("awq_search_scale_noalloc", _int, [_p, _i64, _i64, _i64, _p, _i64, _i64, _p, _p, _int, _int,
                                         _p, _p, _p, _p, _p]),
     ("awq_pack_int4", _int, [_p, _i64, _i64, _i64, _p, _int, _p, _p, _p, _p]),
+    ("awq_pack_int3", _int, [_p, _i64, _i64, _i64, _p, _int, _p, _p, _p, _p]),
     ("w4a16_gemm", _int, [_p, _i64, _i64, _i64, _p, _p, _p, _i64, _int, _p, _i64, _p, _sz, _p]),
     ("w4a16_gemm_workspace_size", _sz, [_i64, _i64, _i64]),
     ("w4a16_gemm_scaled", _int, [_p, _i64, _i64, _i64, _p, _p, _p, _p, _i64, _int, _p, _i64, _p,
@@ -211,6 +213,24 @@ def pack_int4(W: torch.Tensor, s: torch.Tensor | None = None, out=None, stream=N
                                GROUP, qw.data_ptr(), sc.data_ptr(), ze.data_ptr(), _stream(stream)),
            "awq_pack_int4")
     return qw, sc, ze
+
+
+def pack_int3(W: torch.Tensor, s: torch.Tensor | None = None, out=None, stream=None):
+    """3-bit pack of W diag(s): ``(planes int32 [N, 3K/32] (uint32 bits),
+    scales fp16 [N, K/128], zeros fp16 [N, K/128])``."""
+    _dev(W, torch.float16, "W")
+    N, K = W.shape
+    if s is not None:
+        _dev(s, torch.float32, "s")
+    if out is None:
+        out = (torch.empty((N, K // 32 * 3), dtype=torch.int32, device=W.device),
+               torch.empty((N, K // GROUP), dtype=torch.float16, device=W.device),
+               torch.empty((N, K // GROUP), dtype=torch.float16, device=W.device))
+    pl, sc, ze = out
+    _check(lib().awq_pack_int3(W.data_ptr(), N, K, _ld(W), s.data_ptr() if s is not None else None,
+                               GROUP, pl.data_ptr(), sc.data_ptr(), ze.data_ptr(), _stream(stream)),
+           "awq_pack_int3")
+    return pl, sc, ze
 
 
 def w4a16_gemm(X: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,

@@ -11,6 +11,7 @@
 #include "awq.h"
 #include "common.cuh"
 #include "kernels.cuh"
+#include "pack3.cuh"
 
 namespace {
 
@@ -344,6 +345,27 @@ awq_status awq_pack_int4(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, c
     awq_status st_ = device_info(&d);
     if (st_) return st_;
     cudaError_t e = awq::launch_pack_int4(W, N, K, ldw, s, qweight, scales, zeros, d->status,
+                                          d->num_sms, (cudaStream_t)stream);
+    return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
+}
+
+awq_status awq_pack_int3(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, const float* s,
+                         int group, uint32_t* planes, uint16_t* scales, uint16_t* zeros,
+                         awq_stream_t stream) {
+    const CallRange range("awq_pack_int3");
+    if (N < 0 || K < 0) return fail(AWQ_ERR_INVALID_ARG, "pack_int3: negative size");
+    if ((N > 0 && K > 0) && (!W || !planes || !scales || !zeros))
+        return fail(AWQ_ERR_INVALID_ARG, "pack_int3: null pointer");
+    if (group != AWQ_GROUP || K % AWQ_GROUP || ldw < K || ldw % 8)
+        return fail(AWQ_ERR_SHAPE, "pack_int3: need group 128, K % 128 == 0, ldw >= K, ldw % 8 == 0");
+    if ((W && !aligned16(W)) || (s && !aligned16(s)) ||
+        (reinterpret_cast<uintptr_t>(planes) & 3u) || (reinterpret_cast<uintptr_t>(scales) & 1u) ||
+        (reinterpret_cast<uintptr_t>(zeros) & 1u))
+        return fail(AWQ_ERR_ALIGN, "pack_int3: W, s must be 16-byte aligned, planes 4-byte");
+    DevInfo* d = nullptr;
+    awq_status st_ = device_info(&d);
+    if (st_) return st_;
+    cudaError_t e = awq::launch_pack_int3(W, N, K, ldw, s, planes, scales, zeros, d->status,
                                           d->num_sms, (cudaStream_t)stream);
     return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
 }

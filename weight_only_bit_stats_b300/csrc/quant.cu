@@ -7,6 +7,7 @@
 // group of 128 with fp16 scale/zero are the library's stated format.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "pack3.cuh"
 
 namespace awq {
 namespace {
@@ -150,6 +151,110 @@ __global__ void __launch_bounds__(256)
     if (bad) set_status(status, kStatusNonFinite);
 }
 
+// Group parameters at 3 bits: the rule of group_quant_from_range with the
+// top level 7 instead of 15 (d = fp32(range / 7), zero-point clamped to 0..7).
+// The exact-quotient rounding holds unchanged: only quotients below 8 in
+// magnitude can leave the clamp.
+__device__ __forceinline__ GroupQuant group_quant3_from_range(float lo, float hi) {
+    GroupQuant g;
+    const float range = __fsub_rn(hi, lo);
+    float d = __fdiv_rn(range, 7.0f);
+    d = fmaxf(d, 6.103515625e-05f);              // 2^-14, least normal fp16
+    g.scale_h = __float2half_rn(d);
+    g.scale = __half2float(g.scale_h);
+    g.finite = isfinite(g.scale);
+    g.rcp = __frcp_rn(g.scale);
+    const float z = rint_quot(-lo, g.scale, g.rcp);
+    g.zf = z > 0.0f ? fminf(z, 7.0f) : 0.0f;
+    return g;
+}
+
+// 3-bit pack ("3 and 4 bits", AWQ page, fourth paragraph): the layout of
+// pack_int4_kernel's lanes (8 per row-group, 16 channels each), levels
+// 0..7, and three bit planes per 32 levels.  A lane sets bit p of its 16
+// levels in the low or high half of plane word p; the lane pair of a 32-level
+// block ORs its halves and the even lane writes the block's three words.
+__global__ void __launch_bounds__(256)
+    pack_int3_kernel(const uint16_t* __restrict__ W, int64_t N, int64_t K, int64_t ldw,
+                     const float* __restrict__ s, uint32_t* __restrict__ planes,
+                     uint16_t* __restrict__ scales, uint16_t* __restrict__ zeros,
+                     unsigned* status) {
+    const int lane = threadIdx.x & 31, c = lane & 7, rg = lane >> 3;
+    const int64_t G = K / kGroup;
+    const int64_t total = N * G;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    bool bad = false;
+    for (int64_t base = warp0 * 4; base < total; base += nwarps * 4) {
+        const int64_t item = base + rg;
+        const bool live = item < total;
+        const int64_t it = live ? item : total - 1;
+        const int64_t n = it / G, g = it - n * G;
+        const int64_t k0 = g * kGroup + 16 * c;
+        const uint4* wp4 = reinterpret_cast<const uint4*>(W + n * ldw + k0);
+        const uint4 r0 = __ldg(wp4), r1 = __ldg(wp4 + 1);
+        float4 sv[4];
+        if (s) {
+            const float4* sp = reinterpret_cast<const float4*>(s + k0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sv[j] = __ldg(sp + j);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sv[j] = make_float4(1.f, 1.f, 1.f, 1.f);
+        }
+        const uint32_t wr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        const float* sf = reinterpret_cast<const float*>(sv);
+        float wp[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const uint32_t h = (wr[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+            wp[e] = __fmul_rn(__half2float(__ushort_as_half((unsigned short)h)), sf[e]);
+        }
+        float lo = wp[0], hi = wp[0];
+#pragma unroll
+        for (int e = 1; e < 16; ++e) {
+            lo = fmin_nan(lo, wp[e]);
+            hi = fmax_nan(hi, wp[e]);
+        }
+        const bool lane_bad = !(isfinite(lo) && isfinite(hi));
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+        const GroupQuant gq = group_quant3_from_range(lo, hi);
+        if (live) bad |= lane_bad || !gq.finite;
+        float rt[16];
+        rint_quot8(wp, gq.scale, gq.rcp, rt);
+        rint_quot8(wp + 8, gq.scale, gq.rcp, rt + 8);
+        uint32_t p0 = 0, p1 = 0, p2 = 0;
+        const int sh = 16 * (c & 1);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const uint32_t q = (uint32_t)fminf(fmaxf(__fadd_rn(rt[e], gq.zf), 0.0f), 7.0f);
+            p0 |= (q & 1u) << (sh + e);
+            p1 |= ((q >> 1) & 1u) << (sh + e);
+            p2 |= (q >> 2) << (sh + e);
+        }
+        p0 |= __shfl_xor_sync(0xffffffffu, p0, 1);
+        p1 |= __shfl_xor_sync(0xffffffffu, p1, 1);
+        p2 |= __shfl_xor_sync(0xffffffffu, p2, 1);
+        if (live) {
+            if ((c & 1) == 0) {
+                uint32_t* w = planes + n * (K / 32 * 3) + g * 12 + (c >> 1) * 3;
+                w[0] = p0;
+                w[1] = p1;
+                w[2] = p2;
+            }
+            if (c == 0) {
+                scales[n * G + g] = __half_as_ushort(gq.scale_h);
+                zeros[n * G + g] = __half_as_ushort(__float2half_rn(gq.zf));
+            }
+        }
+    }
+    if (bad) set_status(status, kStatusNonFinite);
+}
+
 // mse[a] = (sum of alpha a's partials) / (T N): one warp per alpha, lane-
 // strided fp64 sums added in a fixed butterfly order (deterministic); then
 // the first argmin and its candidate scales.
@@ -246,6 +351,19 @@ cudaError_t launch_pack_int4(const uint16_t* W, int64_t N, int64_t K, int64_t ld
     const int64_t cap = (int64_t)num_sms * 8;
     if (blocks > cap) blocks = cap;
     pack_int4_kernel<<<(unsigned)blocks, 256, 0, st>>>(W, N, K, ldw, s, qweight, scales, zeros,
+                                                       status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_int3(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, const float* s,
+                             uint32_t* planes, uint16_t* scales, uint16_t* zeros, unsigned* status,
+                             int num_sms, cudaStream_t st) {
+    const int64_t items = N * (K / kGroup);
+    if (items == 0) return cudaSuccess;
+    int64_t blocks = (items + 31) / 32;               // 8 warps x 4 row-groups
+    const int64_t cap = (int64_t)num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    pack_int3_kernel<<<(unsigned)blocks, 256, 0, st>>>(W, N, K, ldw, s, planes, scales, zeros,
                                                        status);
     return cudaGetLastError();
 }
