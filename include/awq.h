@@ -176,10 +176,21 @@ awq_status awq_pack_int4(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
  *            level 32 j + i at bit i (exactly 3 bits per weight).
  *   scales   [N, K/128] fp16.     zeros [N, K/128] fp16 holding 0..7.
  * K % 128 == 0; W and s 16-byte aligned, planes 4-byte, scales/zeros 2-byte.
- * No matmul consumes this format yet. */
+ * w3a16_gemm consumes this format. */
 awq_status awq_pack_int3(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
                          const float* s, int group, uint32_t* planes, uint16_t* scales,
                          uint16_t* zeros, awq_stream_t stream);
+
+/* ---- step: 3-bit decode matmul -----------------------------------------------
+ * Y = X deq(Wq)^T over the 3-bit format of awq_pack_int3, deq = (q - z) *
+ * scale, fp32 accumulation, fp16 out, for 1 <= M <= 16 tokens (decoding,
+ * the memory-bound case; AWQ page sixth paragraph: fewer bytes per weight,
+ * faster tokens at small batch).  Arguments as w4a16_gemm, with planes
+ * [N, 3K/32] uint32 in place of qweight.  M > 16 returns AWQ_ERR_SHAPE.
+ * X 16-byte aligned, ldx a multiple of 8; planes 4-byte aligned. */
+awq_status w3a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
+                      const uint32_t* planes, const uint16_t* scales, const uint16_t* zeros,
+                      int64_t N, int group, uint16_t* Y, int64_t ldy, awq_stream_t stream);
 
 /* ---- step: dequantise-fused matmul -----------------------------------------
  * Y = X deq(Wq)^T, deq = (q - z) * scale, fp32 accumulation, fp16 out

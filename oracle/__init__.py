@@ -321,6 +321,22 @@ def search_scale(W: np.ndarray, X: np.ndarray, m: np.ndarray,
 
 # ---- steps a6/a7: the dequantised matmul --------------------------------
 
+def w3a16_gemm(X: np.ndarray, planes: np.ndarray, scales: np.ndarray,
+               zeros: np.ndarray, row_chunk: int = 4096) -> np.ndarray:
+    """Y = X deq(Wq)^T in fp64 over the 3-bit planes of ``pack_int3``."""
+    X64 = h2d(X)
+    M, K = X64.shape
+    N = planes.shape[0]
+    G = K // GROUP
+    Y = np.empty((M, N), dtype=np.float64)
+    for n0 in range(0, N, row_chunk):
+        n1 = min(N, n0 + row_chunk)
+        q = unpack_planes3(planes[n0:n1], K)
+        D = dequant(q, _bits(scales)[n0:n1].reshape(-1, G), _bits(zeros)[n0:n1].reshape(-1, G))
+        Y[:, n0:n1] = X64 @ D.T
+    return Y
+
+
 def w4a16_gemm(X: np.ndarray, qweight: np.ndarray, scales: np.ndarray,
                zeros: np.ndarray, row_chunk: int = 4096) -> np.ndarray:
     """Y = X deq(Wq)^T in fp64, [M, N]."""

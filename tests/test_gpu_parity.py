@@ -186,6 +186,32 @@ def test_pack_int3_edge_groups(wb, orc):
     assert e.value.code == 8
 
 
+@pytest.mark.parametrize("M", [1, 3, 8, 16])
+@pytest.mark.parametrize("N,K", [(64, 128), (136, 384), (1024, 1024), (520, 2304)])
+def test_w3a16_decode_parity(wb, orc, M, N, K):
+    """The 3-bit decode matmul on the GPU's own 3-bit pack: the planes match
+    the oracle's bit for bit, and Y is within the matmul bar of fp64."""
+    W, _, X, _ = sg.layer_inputs(17, 0, N, K, 0, M=M)
+    pl, sc, ze = wb.pack_int3(dev(W))
+    rp, rs, rz = orc.pack_int3(W)
+    assert np.array_equal(u32(pl), rp)
+    Y = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    wb.w3a16_gemm(dev(X), pl, sc, ze, out=Y)
+    y = host(Y)
+    assert np.all(np.isfinite(y))
+    assert rel_err(y, orc.w3a16_gemm(X, rp, rs, rz)) <= GEMM_TOL
+    wb.sync_status()
+
+
+def test_w3a16_refuses_prefill_sizes(wb):
+    x = torch.zeros((17, 128), dtype=torch.float16, device="cuda")
+    pl = torch.zeros((8, 12), dtype=torch.int32, device="cuda")
+    sc = torch.zeros((8, 1), dtype=torch.float16, device="cuda")
+    with pytest.raises(wb.AwqError) as e:
+        wb.w3a16_gemm(x, pl, sc, sc)
+    assert e.value.code == 2
+
+
 # ---------------------------------------------------------- a2-a4 search --
 
 def _search_check(wb, orc, W, X, alphas=None):

@@ -577,3 +577,13 @@ def test_gram_route_exact_tiny(oracle_mod):
     exact = float(total / 6)
     g = oracle_mod.search_mse_gram(W, oracle_mod.gram(X), 3, s)
     assert abs(g - exact) <= 1e-12 * exact
+
+
+def test_w3a16_matches_the_nibble_route(oracle_mod):
+    """Levels 0..7 stored as bit planes or as nibbles dequantise to the same
+    weights: the 3-bit matmul equals the (pinned) 4-bit one on them."""
+    W, _, X, _ = sg.layer_inputs(6, 0, 40, 384, 0, M=5)
+    q, sc, ze = oracle_mod.quantize(W, None, bits=3)
+    y3 = oracle_mod.w3a16_gemm(X, oracle_mod.pack_planes3(q), sc, ze)
+    y4 = oracle_mod.w4a16_gemm(X, oracle_mod.pack_nibbles(q), sc, ze)
+    assert np.array_equal(y3, y4)

@@ -21,7 +21,8 @@ import os
 import torch
 
 __all__ = ["AwqError", "lib", "act_stats", "act_mean", "candidate_scales", "search_scale",
-           "pack_int4", "pack_int3", "w4a16_gemm", "w4a16_gemm_scaled", "set_weight_prefetch",
+           "pack_int4", "pack_int3", "w4a16_gemm", "w3a16_gemm", "w4a16_gemm_scaled",
+           "set_weight_prefetch",
            "sync_status",
            "ALPHA_GRID",
            "GROUP"]
@@ -60,6 +61,7 @@ SIGNATURES = (
                                         _p, _p, _p, _p, _p]),
     ("awq_pack_int4", _int, [_p, _i64, _i64, _i64, _p, _int, _p, _p, _p, _p]),
     ("awq_pack_int3", _int, [_p, _i64, _i64, _i64, _p, _int, _p, _p, _p, _p]),
+    ("w3a16_gemm", _int, [_p, _i64, _i64, _i64, _p, _p, _p, _i64, _int, _p, _i64, _p]),
     ("w4a16_gemm", _int, [_p, _i64, _i64, _i64, _p, _p, _p, _i64, _int, _p, _i64, _p, _sz, _p]),
     ("w4a16_gemm_workspace_size", _sz, [_i64, _i64, _i64]),
     ("w4a16_gemm_scaled", _int, [_p, _i64, _i64, _i64, _p, _p, _p, _p, _i64, _int, _p, _i64, _p,
@@ -231,6 +233,23 @@ def pack_int3(W: torch.Tensor, s: torch.Tensor | None = None, out=None, stream=N
                                GROUP, pl.data_ptr(), sc.data_ptr(), ze.data_ptr(), _stream(stream)),
            "awq_pack_int3")
     return pl, sc, ze
+
+
+def w3a16_gemm(X: torch.Tensor, planes: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,
+               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y = X deq(Wq)^T over the 3-bit planes of ``pack_int3``, fp16 [M, N],
+    M <= 16."""
+    _dev(X, torch.float16, "X")
+    _dev(planes, torch.int32, "planes")
+    _dev(scales, torch.float16, "scales")
+    _dev(zeros, torch.float16, "zeros")
+    M, K = X.shape
+    N = planes.shape[0]
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=X.device)
+    _check(lib().w3a16_gemm(X.data_ptr(), M, K, _ld(X), planes.data_ptr(), scales.data_ptr(),
+                            zeros.data_ptr(), N, GROUP, Y.data_ptr(), _ld(Y), _stream(stream)),
+           "w3a16_gemm")
+    return Y
 
 
 def w4a16_gemm(X: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,

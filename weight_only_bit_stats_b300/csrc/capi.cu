@@ -11,7 +11,7 @@
 #include "awq.h"
 #include "common.cuh"
 #include "kernels.cuh"
-#include "pack3.cuh"
+#include "int3.cuh"
 
 namespace {
 
@@ -346,6 +346,30 @@ awq_status awq_pack_int4(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, c
     if (st_) return st_;
     cudaError_t e = awq::launch_pack_int4(W, N, K, ldw, s, qweight, scales, zeros, d->status,
                                           d->num_sms, (cudaStream_t)stream);
+    return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
+}
+
+awq_status w3a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
+                      const uint32_t* planes, const uint16_t* scales, const uint16_t* zeros,
+                      int64_t N, int group, uint16_t* Y, int64_t ldy, awq_stream_t stream) {
+    const CallRange range("w3a16_gemm");
+    if (M < 0 || N < 0 || K < 0) return fail(AWQ_ERR_INVALID_ARG, "w3a16_gemm: negative size");
+    if (M == 0 || N == 0) return AWQ_OK;
+    if (!X || !planes || !scales || !zeros || !Y)
+        return fail(AWQ_ERR_INVALID_ARG, "w3a16_gemm: null pointer");
+    if (M > 16 || group != AWQ_GROUP || K <= 0 || K % AWQ_GROUP || N % 8 || ldx < K || ldx % 8 ||
+        ldy < N)
+        return fail(AWQ_ERR_SHAPE, "w3a16_gemm: need M <= 16, group 128, K % 128 == 0, N % 8 == 0, ldx >= K, ldx % 8 == 0, ldy >= N");
+    if (N > (1LL << 30) || K > (1LL << 30)) return fail(AWQ_ERR_SHAPE, "w3a16_gemm: size too large");
+    if (!aligned16(X) || (reinterpret_cast<uintptr_t>(planes) & 3u) ||
+        (reinterpret_cast<uintptr_t>(Y) & 1u) || (reinterpret_cast<uintptr_t>(scales) & 1u) ||
+        (reinterpret_cast<uintptr_t>(zeros) & 1u))
+        return fail(AWQ_ERR_ALIGN, "w3a16_gemm: X must be 16-byte aligned, planes 4-byte");
+    DevInfo* d = nullptr;
+    awq_status st_ = device_info(&d);
+    if (st_) return st_;
+    cudaError_t e = awq::launch_gemv_w3a16(X, ldx, (int)M, planes, scales, zeros, N, K, Y, ldy,
+                                           d->num_sms, (cudaStream_t)stream);
     return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
 }
 

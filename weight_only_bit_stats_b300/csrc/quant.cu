@@ -7,7 +7,7 @@
 // group of 128 with fp16 scale/zero are the library's stated format.
 #include "common.cuh"
 #include "kernels.cuh"
-#include "pack3.cuh"
+#include "int3.cuh"
 
 namespace awq {
 namespace {
