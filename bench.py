@@ -47,10 +47,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # DRAM traffic of the fused search kernel, dram__bytes_read.sum +
 # dram__bytes_write.sum summed over the four search launches of one step of
 # this workload in one ncu capture (profiles/tc_search_llama7b_qkv.md),
-# valid only while the kernel's sources are the ones captured.
+# valid only while the kernel's sources (comments aside) are the ones
+# captured.
 SEARCH_TRAFFIC = {"bytes_per_step": 105571584 + 2872320 + 38458624 + 0 + 185359104 + 186624 +
                                     103278080 + 148224,
-                  "src_sha": "09baa005635d0117"}
+                  "src_sha": "0bb1a084ee3f3856"}
 SEARCH_SOURCES = ("tc.cu", "common.cuh", "kernels.cuh")
 
 
@@ -70,11 +71,39 @@ def load_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+def strip_comments(text):
+    """C/C++/CUDA source without its comments, trailing blanks and empty
+    lines: the part of a kernel's source that its counters depend on.
+    String and character literals are kept as they are."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            while i < n and text[i] != "\n":
+                i += 1
+        elif text.startswith("/*", i):
+            end = text.find("*/", i + 2)
+            i = n if end < 0 else end + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).split("\n"))
+    return "\n".join(line for line in lines if line)
+
+
 def src_sha(names):
+    """Hash of the named kernel sources, comments and layout excluded."""
     import hashlib
     h = hashlib.sha256()
     for name in names:
-        h.update(open(os.path.join(ROOT, "weight_only_bit_stats_b300", "csrc", name), "rb").read())
+        path = os.path.join(ROOT, "weight_only_bit_stats_b300", "csrc", name)
+        h.update(strip_comments(open(path).read()).encode())
     return h.hexdigest()[:16]
 
 

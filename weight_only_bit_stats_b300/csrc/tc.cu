@@ -256,7 +256,7 @@ __device__ void role_epilogue(const TcParams& p, SmemCtl* ctl, uint32_t tmem, in
     }
 }
 
-// ---- role: GEMM weight producer (int4 -> exact fp16 (q - z) * scale) ----
+// ---- role: GEMM weight producer (int4 -> fp16 (q - z) * scale) ----
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t d;
     asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
@@ -270,8 +270,10 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
-// 8 nibbles -> 8 consecutive fp16 (q - z) * scale, exact (|q - z| <= 15 and
-// an 11-bit scale significand give at most 15 significant bits).
+// 8 nibbles -> 8 consecutive fp16 values of (q - z) * scale.  (q - z), an
+// integer in [-15, 15], is exact in fp16; its product with the fp16 scale can
+// need up to 15 significant bits and is rounded once to fp16 (relative error
+// at most 2^-11, the rounding an fp16 weight carries anyway).
 __device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 z1024, __half2 zneg64, __half2 sc) {
     const uint32_t magic = 0x64006400u;
     const __half2 sixteenth = __half2half2(__float2half_rn(0.0625f));
