@@ -7,12 +7,16 @@
 // (sixth paragraph).  This first 3-bit kernel is plain CUDA-core code:
 //
 //  * One warp per output row at a time; lane l takes the row's 32-level
-//    blocks l, l + 32, ... (three plane words each, three coalesced 4-byte
-//    loads per warp step).
-//  * A block's 32 levels are rebuilt from the three planes, turned into the
-//    exact fp32 values (q - z) * scale (at most 3 + 11 significant bits),
-//    and multiplied into every token's accumulator with fp32 FMAs; the
-//    activations come through L1 as 16-byte loads.
+//    blocks l, l + 32, ..., four at a time: the plane words, scales and
+//    zero-points of four blocks are requested before any is used, so a row
+//    costs one memory round trip per four blocks rather than per block.
+//  * Levels i and i + 16 of a block sit at bits i and i + 16 of each plane,
+//    so three shifts and three LOP3s place both levels' bits under the
+//    mantissa of fp16 1024 at once; one HSUB2 gives the exact pair
+//    (q - z), which is widened and scaled to the exact fp32 values
+//    (q - z) * scale (at most 3 + 11 significant bits) and multiplied into
+//    every token's accumulator with fp32 FMAs.  The activations come
+//    through L1 as 16-byte loads.
 //  * The 32 lanes' sums are added in a fixed butterfly order, so the result
 //    is deterministic.
 #include "common.cuh"
@@ -22,6 +26,41 @@ namespace awq {
 namespace {
 
 constexpr int kW3Warps = 8;
+constexpr int kW3Batch = 4;                  // blocks a lane loads at once
+
+__device__ __forceinline__ uint32_t lop3_or_and(uint32_t a, uint32_t mask, uint32_t c) {
+    uint32_t d;      // (a & mask) | c
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(c));
+    return d;
+}
+
+// Bits i and i + 16 of plane p, moved to bits p and 16 + p.
+template <int I, int P>
+__device__ __forceinline__ uint32_t plane_bits(uint32_t w) {
+    if constexpr (I >= P) return w >> (I - P);
+    else return w << (P - I);
+}
+
+// The exact fp32 weights (q - z) * sc of levels I and I + 16 of a block.
+template <int I>
+__device__ __forceinline__ void level_pair(uint32_t p0, uint32_t p1, uint32_t p2,
+                                           __half2 z1024, float sc, float& wa, float& wb) {
+    uint32_t v = lop3_or_and(plane_bits<I, 0>(p0), 0x00010001u, 0x64006400u);
+    v = lop3_or_and(plane_bits<I, 1>(p1), 0x00020002u, v);
+    v = lop3_or_and(plane_bits<I, 2>(p2), 0x00040004u, v);
+    const float2 d = __half22float2(__hsub2(*reinterpret_cast<const __half2*>(&v), z1024));
+    wa = __fmul_rn(d.x, sc);
+    wb = __fmul_rn(d.y, sc);
+}
+
+template <int I>
+__device__ __forceinline__ void block_weights(uint32_t p0, uint32_t p1, uint32_t p2,
+                                              __half2 z1024, float sc, float (&w)[32]) {
+    if constexpr (I < 16) {
+        level_pair<I>(p0, p1, p2, z1024, sc, w[I], w[I + 16]);
+        block_weights<I + 1>(p0, p1, p2, z1024, sc, w);
+    }
+}
 
 template <int MT>
 __global__ void __launch_bounds__(kW3Warps * 32, 2)
@@ -39,20 +78,29 @@ __global__ void __launch_bounds__(kW3Warps * 32, 2)
 #pragma unroll
         for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
         const uint32_t* prow = planes + n * nb * 3;
-        for (int64_t j = lane; j < nb; j += 32) {
-            const uint32_t p0 = __ldg(prow + j * 3);
-            const uint32_t p1 = __ldg(prow + j * 3 + 1);
-            const uint32_t p2 = __ldg(prow + j * 3 + 2);
-            const int64_t g = j >> 2;              // 4 blocks per group of 128
-            const float sc = __half2float(__ushort_as_half(__ldg(scales + n * G + g)));
-            const float z = __half2float(__ushort_as_half(__ldg(zeros + n * G + g)));
-            float w[32];
+        for (int64_t j0 = lane; j0 < nb; j0 += 32 * kW3Batch) {
+            uint32_t pw[kW3Batch][3];
+            uint16_t sb[kW3Batch], zb[kW3Batch];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const uint32_t q = ((p0 >> i) & 1u) | (((p1 >> i) & 1u) << 1) |
-                                   (((p2 >> i) & 1u) << 2);
-                w[i] = __fmul_rn(__fsub_rn((float)q, z), sc);   // exact
+            for (int b = 0; b < kW3Batch; ++b) {
+                const int64_t j = j0 + 32 * b;
+                if (j < nb) {
+                    pw[b][0] = __ldg(prow + j * 3);
+                    pw[b][1] = __ldg(prow + j * 3 + 1);
+                    pw[b][2] = __ldg(prow + j * 3 + 2);
+                    sb[b] = __ldg(scales + n * G + (j >> 2));   // 4 blocks per group
+                    zb[b] = __ldg(zeros + n * G + (j >> 2));
+                }
             }
+#pragma unroll
+            for (int b = 0; b < kW3Batch; ++b) {
+            const int64_t j = j0 + 32 * b;
+            if (j >= nb) break;
+            const float sc = __half2float(__ushort_as_half(sb[b]));
+            const __half2 z1024 =
+                __half2half2(__hadd(__float2half_rn(1024.0f), __ushort_as_half(zb[b])));
+            float w[32];
+            block_weights<0>(pw[b][0], pw[b][1], pw[b][2], z1024, sc, w);
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 if (m < M) {
@@ -69,6 +117,7 @@ __global__ void __launch_bounds__(kW3Warps * 32, 2)
                         }
                     }
                 }
+            }
             }
         }
 #pragma unroll
