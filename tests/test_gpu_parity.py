@@ -203,6 +203,21 @@ def test_w3a16_decode_parity(wb, orc, M, N, K):
     wb.sync_status()
 
 
+@pytest.mark.parametrize("M,N,K", [(16, 64, 7168), (8, 40, 13824)])
+def test_w3a16_decode_long_k(wb, orc, M, N, K):
+    """Activations too large to stage in shared memory take the CUDA-core
+    kernel; the same parity bar."""
+    W, _, X, _ = sg.layer_inputs(17, 1, N, K, 0, M=M)
+    rp, rs, rz = orc.pack_int3(W)
+    Y = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    wb.w3a16_gemm(dev(X), dev(rp.view(np.int32)), dev(rs.view(np.float16)),
+                  dev(rz.view(np.float16)), out=Y)
+    y = host(Y)
+    assert np.all(np.isfinite(y))
+    assert rel_err(y, orc.w3a16_gemm(X, rp, rs, rz)) <= GEMM_TOL
+    wb.sync_status()
+
+
 def test_w3a16_refuses_prefill_sizes(wb):
     x = torch.zeros((17, 128), dtype=torch.float16, device="cuda")
     pl = torch.zeros((8, 12), dtype=torch.int32, device="cuda")
