@@ -233,6 +233,46 @@ def test_quantizer_edge_groups(oracle_mod):
     _check_nearest(oracle_mod, W[3:6], None)
 
 
+def _golden_groups():
+    """Lines of the hand-derived group fixture: (bits, group weights, scale
+    bits, zero-point, [(position, level), ...])."""
+    out = []
+    for line in open(os.path.join(GOLDEN, "quant_groups.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        head, vals, levels = line.split("|")
+        bits, fill = head.split()
+        vals, expect = vals.split("->")
+        ws = [float(v) for v in vals.split()]
+        sc_bits, zero = expect.split()
+        qs = [int(v) for v in levels.split()]
+        assert len(qs) == len(ws)
+        g = np.full(128, float(fill))
+        g[:len(ws)] = ws
+        assert np.array_equal(g.astype(np.float16).astype(np.float64), g)   # exact in fp16
+        out.append((int(bits), g.astype(np.float16)[None, :], int(sc_bits, 16), int(zero),
+                    list(enumerate(qs))))
+    return out
+
+
+def test_quantizer_golden_groups(oracle_mod):
+    """Stored scale, zero-point and levels of hand-derived groups
+    (tests/golden/quant_groups.txt): the scale is the NEAREST fp16 to
+    range/qmax (lines where truncation, or rounding up, gives another fp16,
+    one of them crossing a binade), the zero-point is rint of -lo/scale (lines
+    where floor, ceil, or ties away from zero give another integer), and the
+    clamps of a one-signed group; at 4 and 3 bits."""
+    groups = _golden_groups()
+    assert len(groups) >= 8 and {b for b, *_ in groups} == {3, 4}
+    for bits, w, sc_bits, zero, levels in groups:
+        q, sc, ze = oracle_mod.quantize(w, None, bits=bits)
+        assert int(sc[0, 0]) == sc_bits, (bits, w[0, :4], hex(int(sc[0, 0])))
+        assert ze.view(np.float16)[0, 0] == zero and int(ze[0, 0]) == oracle_mod.d2h_rn(zero)
+        for pos, lev in levels:
+            assert int(q[0, pos]) == lev, (bits, w[0, pos], int(q[0, pos]), lev)
+
+
 def test_quantizer_nonfinite_rejected(oracle_mod):
     W = np.zeros((1, 128), dtype=np.float16)
     W[0, 5] = np.inf
