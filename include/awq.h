@@ -54,7 +54,8 @@ enum {
     AWQ_ERR_WORKSPACE = 5,   /* workspace missing or too small */
     AWQ_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed */
     AWQ_ERR_TIMEOUT = 7,     /* a bounded device-side wait expired */
-    AWQ_ERR_NONFINITE = 8    /* NaN/Inf input, or a group scale overflowing fp16 */
+    AWQ_ERR_NONFINITE = 8,   /* NaN/Inf input, or a group scale overflowing fp16 */
+    AWQ_ERR_OVERFLOW = 9     /* an accumulated statistics sum left the exact int64 range */
 };
 
 /* Same type as cudaStream_t. */
@@ -71,9 +72,14 @@ typedef struct CUstream_st* awq_stream_t;
  *   accumulate   0: abs_sum_q24 is overwritten; 1: this batch is added to
  *                it (stream calibration batches through one buffer).
  *   abs_sum_q24  [K] int64: sum_t |X[t,k]| * 2^24.  Every finite fp16 is an
- *                integer multiple of 2^-24, so the sums are exact integers
- *                and independent of summation order (bit-reproducible) for
- *                fewer than 2^23 tokens in total.
+ *                integer multiple of 2^-24 below 2^16, so the sums are exact
+ *                integers and independent of summation order
+ *                (bit-reproducible) while the running total stays below 2^63,
+ *                which any 2^23 - 1 tokens guarantee.
+ * T must be below 2^23 (AWQ_ERR_SHAPE otherwise).  With accumulate = 1 the
+ * caller keeps the total token count of all batches below 2^23 for the same
+ * guarantee; a running total that reaches 2^63 anyway flags AWQ_ERR_OVERFLOW
+ * in the status word (the sums are then invalid).
  * NaN/Inf inputs are skipped and flag AWQ_ERR_NONFINITE in the status word. */
 awq_status awq_act_stats(const uint16_t* X, int64_t T, int64_t K, int64_t ldx,
                          int accumulate, int64_t* abs_sum_q24, awq_stream_t stream);
@@ -134,9 +140,11 @@ size_t awq_search_workspace_size(int64_t N, int64_t K, int64_t T, int n_alpha);
  * library-owned device array of AWQ_SEARCH_NOALLOC_SCRATCH_BYTES that every
  * GPU loading the library holds until the process exits.  Problems whose
  * awq_search_workspace_size() exceeds that size are refused with
- * AWQ_ERR_WORKSPACE.  The first call on a device looks up the array's device
- * address (make that first call before any stream capture).  All calls share
- * the array: calls that overlap on the GPU race. */
+ * AWQ_ERR_WORKSPACE (bad sizes or n_alpha are AWQ_ERR_INVALID_ARG first).
+ * The first call on a device looks up the array's device address (make that
+ * first call before any stream capture); a call in a context other than the
+ * one of that lookup (e.g. after cudaDeviceReset) looks it up again.  All
+ * calls share the array: calls that overlap on the GPU race. */
 #define AWQ_SEARCH_NOALLOC_SCRATCH_BYTES (16u << 20)
 awq_status awq_search_scale_noalloc(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
                                     const uint16_t* Xcal, int64_t T, int64_t ldx,
@@ -251,9 +259,10 @@ awq_status awq_set_weight_prefetch(int enable);
 /* ---- status and diagnostics ---------------------------------------------- */
 
 /* Synchronise `stream`, then return (and clear) the device-side status word
- * of the current device: AWQ_OK, AWQ_ERR_NONFINITE or AWQ_ERR_TIMEOUT
- * (the most severe seen since the last call), or AWQ_ERR_CUDA if the
- * synchronisation itself failed. */
+ * of the current device: AWQ_OK, AWQ_ERR_NONFINITE, AWQ_ERR_OVERFLOW or
+ * AWQ_ERR_TIMEOUT (the most severe seen since the last call, in the order
+ * timeout, overflow, non-finite), or AWQ_ERR_CUDA if the synchronisation
+ * itself failed. */
 awq_status awq_sync_status(awq_stream_t stream);
 
 /* Diagnostic of the failure path (no counterpart on the AWQ pages): every

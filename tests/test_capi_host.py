@@ -76,6 +76,9 @@ def test_host_argument_checks(capi):
                                  None, base, None, None, 0, None) == 5
     # stats: bad accumulate flag
     assert capi.awq_act_stats(base, 4, 128, 128, 2, base, None) == 1
+    # stats: the exact int64 sums hold for fewer than 2^23 tokens per call
+    assert capi.awq_act_stats(base, 1 << 23, 128, 128, 0, base, None) == 2
+    assert capi.awq_act_stats(base, 1 << 23, 128, 128, 1, base, None) == 2
     # decode weight prefetch: a flag, 0 or 1 only (host-side setting)
     assert capi.awq_set_weight_prefetch(2) == 1
     assert capi.awq_set_weight_prefetch(1) == 0 and capi.awq_set_weight_prefetch(0) == 0

@@ -84,6 +84,23 @@ def test_act_stats_nonfinite_flag(wb):
     wb.sync_status()     # cleared
 
 
+def test_act_stats_running_total_overflow_flag(wb):
+    """A streamed total that reaches 2^63 (beyond the exact int64 range) is
+    reported as AWQ_ERR_OVERFLOW; a total just below it is not."""
+    X = np.full((4, 128), 65504.0, dtype=np.float16)      # |x| 2^24 = 65504 * 2^24 each
+    per_col = 4 * 65504 * (1 << 24)
+    acc = torch.full((128,), (1 << 63) - 1 - per_col, dtype=torch.int64, device="cuda")
+    wb.act_stats(dev(X), acc)
+    wb.sync_status()                                      # exactly 2^63 - 1: still exact
+    assert int(host(acc)[5]) == (1 << 63) - 1
+    acc = torch.full((128,), (1 << 63) - per_col, dtype=torch.int64, device="cuda")
+    wb.act_stats(dev(X), acc)
+    with pytest.raises(wb.AwqError) as e:
+        wb.sync_status()
+    assert e.value.code == 9
+    wb.sync_status()     # cleared
+
+
 # ------------------------------------------------------------------ a2 ----
 
 @pytest.mark.parametrize("K", [128, 4096, 11008])

@@ -34,7 +34,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libawq_b300.so")
 
 _STATUS = {0: "AWQ_OK", 1: "AWQ_ERR_INVALID_ARG", 2: "AWQ_ERR_SHAPE", 3: "AWQ_ERR_ALIGN",
            4: "AWQ_ERR_DEVICE", 5: "AWQ_ERR_WORKSPACE", 6: "AWQ_ERR_CUDA", 7: "AWQ_ERR_TIMEOUT",
-           8: "AWQ_ERR_NONFINITE"}
+           8: "AWQ_ERR_NONFINITE", 9: "AWQ_ERR_OVERFLOW"}
 
 
 class AwqError(RuntimeError):

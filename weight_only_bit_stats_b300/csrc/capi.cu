@@ -39,6 +39,7 @@ struct DevInfo {
     bool ok = false;
     int num_sms = 0;
     unsigned* status = nullptr;
+    unsigned long long ctx_id = 0;   // context the status address belongs to
 };
 DevInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -56,15 +57,25 @@ awq_status cuda_fail(cudaError_t e) {
     return AWQ_ERR_CUDA;
 }
 
-// Current device's info; checks compute capability 10.3 once per device.
+// Driver entry points for the context id (the library links the runtime
+// statically and reaches the driver through the runtime's entry-point query).
+using PfnCtxGetCurrent = CUresult (*)(CUcontext*);
+using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+PfnCtxGetCurrent g_ctx_get_current = nullptr;
+PfnCtxGetId g_ctx_get_id = nullptr;
+std::once_flag g_ctx_once;
+
+// Current device's info; checks compute capability 10.3 once per device and
+// context, and looks the status word's address up again in a new context.
 awq_status device_info(DevInfo** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
     if (dev < 0 || dev >= kMaxDevices) return fail(AWQ_ERR_DEVICE, "device index out of range");
+    const unsigned long long ctx = awq::context_id();
     std::lock_guard<std::mutex> lk(g_dev_mu);
     DevInfo& d = g_dev[dev];
-    if (!d.init) {
+    if (!d.init || (ctx != 0 && ctx != d.ctx_id)) {
         d.init = true;
         int major = 0, minor = 0;
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
@@ -75,6 +86,7 @@ awq_status device_info(DevInfo** out) {
         d.status = static_cast<unsigned*>(p);
         d.ok = (major == 10 && minor == 3 && e == cudaSuccess && d.status != nullptr);
         if (e != cudaSuccess) cudaGetLastError();
+        d.ctx_id = awq::context_id();   // the lookup above made the context current
     }
     if (!d.ok) return fail(AWQ_ERR_DEVICE, "requires a compute capability 10.3 (sm_103a) device");
     *out = &d;
@@ -155,6 +167,28 @@ namespace awq {
 // Lets other translation units of the library report an error message
 // through awq_last_error_string().
 awq_status report_error(awq_status code, const char* msg) { return fail(code, msg); }
+
+unsigned long long context_id() {
+    std::call_once(g_ctx_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<PfnCtxGetCurrent>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<PfnCtxGetId>(fn);
+    });
+    if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+    CUcontext c = nullptr;
+    if (g_ctx_get_current(&c) != CUDA_SUCCESS || !c) return 0;
+    unsigned long long id = 0;
+    if (g_ctx_get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 }  // namespace awq
 
 extern "C" {
@@ -197,6 +231,8 @@ awq_status awq_sync_status(awq_stream_t stream) {
         if (e != cudaSuccess) return cuda_fail(e);
     }
     if (v & awq::kStatusTimeout) return fail(AWQ_ERR_TIMEOUT, "a bounded device wait expired");
+    if (v & awq::kStatusOverflow)
+        return fail(AWQ_ERR_OVERFLOW, "an accumulated statistics sum reached 2^63 (too many tokens)");
     if (v & awq::kStatusNonFinite) return fail(AWQ_ERR_NONFINITE, "non-finite value on the device");
     return AWQ_OK;
 }
@@ -208,6 +244,8 @@ awq_status awq_act_stats(const uint16_t* X, int64_t T, int64_t K, int64_t ldx, i
         return fail(AWQ_ERR_INVALID_ARG, "act_stats: negative size or bad accumulate flag");
     if (!abs_sum_q24 || (T > 0 && !X)) return fail(AWQ_ERR_INVALID_ARG, "act_stats: null pointer");
     if (K % 8 || ldx < K || ldx % 8) return fail(AWQ_ERR_SHAPE, "act_stats: K and ldx must be multiples of 8, ldx >= K");
+    if (T >= (1LL << 23))
+        return fail(AWQ_ERR_SHAPE, "act_stats: T must be below 2^23 tokens per call (exact int64 sums)");
     if ((X && !aligned16(X)) || (reinterpret_cast<uintptr_t>(abs_sum_q24) & 7u))
         return fail(AWQ_ERR_ALIGN, "act_stats: X must be 16-byte aligned");
     DevInfo* d = nullptr;

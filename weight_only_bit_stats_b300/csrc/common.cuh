@@ -18,6 +18,7 @@ constexpr int kGroup = 128;
 // Bits of the device status word (see awq_sync_status).
 constexpr unsigned kStatusNonFinite = 1u;
 constexpr unsigned kStatusTimeout = 2u;
+constexpr unsigned kStatusOverflow = 4u;
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -359,19 +360,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Host: raise a kernel's dynamic shared-memory limit once per device.  The
-// attribute call is driver work on the launch path; repeating it per launch
-// adds host latency that a short kernel cannot hide.
+// Host: unique id of the calling thread's current CUDA context, 0 when it
+// has none yet (defined in capi.cu).  Unlike a device ordinal or a context
+// handle, an id is never reused within the process, so state that belongs
+// to one context (symbol addresses, function attributes) is keyed on it and
+// is looked up again in the new primary context after a cudaDeviceReset.
+unsigned long long context_id();
+
+// Host: raise a kernel's dynamic shared-memory limit once per device and
+// context.  The attribute call is driver work on the launch path; repeating
+// it per launch adds host latency that a short kernel cannot hide.
 template <auto Kernel>
 inline cudaError_t smem_attr_once(int bytes) {
-    static std::atomic<unsigned long long> done{0};
+    static std::atomic<unsigned long long> done_ctx[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    const unsigned long long id = context_id();
+    if (id != 0 && done_ctx[dev & 63].load(std::memory_order_acquire) == id) return cudaSuccess;
     e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+    if (e == cudaSuccess) done_ctx[dev & 63].store(context_id(), std::memory_order_release);
     return e;
 }
 

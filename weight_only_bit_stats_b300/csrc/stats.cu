@@ -4,7 +4,7 @@
 //
 // Every finite fp16 value is an integer multiple of 2^-24 below 2^16, so
 // |x| * 2^24 is an integer below 2^40 and the per-channel sum is accumulated
-// exactly in 64-bit integers.  Integer addition is associative, so the
+// exactly in 64-bit integers: any 2^23 - 1 tokens sum to less than 2^63.  Integer addition is associative, so the
 // result is bit-identical whatever the order of threads, blocks or atomics.
 #include "common.cuh"
 #include "kernels.cuh"
@@ -66,7 +66,13 @@ __global__ void __launch_bounds__(kStatCols)
         unsigned long long s = 0;
 #pragma unroll
         for (int y = 0; y < kStatRowLanes; ++y) s += red[y][threadIdx.x];
-        if (s) atomicAdd(abs_sum + col, s);
+        // the running total must stay below 2^63 (a non-negative int64);
+        // a call adds less than 2^63 (fewer than 2^23 tokens, each term
+        // below 2^40), so reaching bit 63 or wrapping is detected here
+        if (s) {
+            const unsigned long long old = atomicAdd(abs_sum + col, s);
+            if (old + s < old || ((old + s) >> 63)) set_status(status, kStatusOverflow);
+        }
     }
     if (bad) set_status(status, kStatusNonFinite);
 }
