@@ -6,8 +6,9 @@ projections (fused qkv 12288x4096, o 4096x4096, fused gate+up 22016x4096,
 down 4096x11008), fp16 weights ~ N(0, 0.02^2), activations ~ N(0,1) with 1%
 of input channels x20, quantised to INT4 g128 by the AWQ search on 512
 calibration tokens.  One step = the whole hot path on every projection:
-act_stats -> act_mean -> search_scale (20 alphas) -> pack_int4, then an L2
-flush, then w4a16_gemm at M = 1 on every projection.
+act_stats -> act_mean -> search_scale (20 alphas) -> pack_int4 ->
+repack_int4 (contiguous decode tiles), then an L2 flush, then the M = 1
+decode matmul (w4a16_gemm_repacked) on every projection.
 
 Headline ``value``: W4A16 GEMV HBM GB/s at M = 1, i.e. the algorithmic bytes
 of the four decode matmuls (packed weights + scales/zeros + x + y) over
@@ -219,6 +220,8 @@ def run_ours(args, rank, world):
         p["sc"] = torch.empty((N, K // 128), dtype=torch.float16, device=dev)
         p["ze"] = torch.empty((N, K // 128), dtype=torch.float16, device=dev)
         p["y"] = torch.empty((1, N), dtype=torch.float16, device=dev)
+        p["tiles"] = torch.empty(wb.lib().awq_repack_int4_bytes(N, K), dtype=torch.uint8,
+                                 device=dev)
     # Decode matmuls may fetch their packed weights before the previous kernel
     # in the stream completes: in this step the first decode launch follows
     # the L2 flush kernels and each other one follows a decode launch (in the
@@ -243,6 +246,7 @@ def run_ours(args, rank, world):
                             out=(p["s"], p["mse"], p["best"]))
             if ev: ev[i][3].record(stream)
             wb.pack_int4(p["W"], p["s"], out=(p["qw"], p["sc"], p["ze"]))
+            wb.repack_int4(p["qw"], p["sc"], p["ze"], out=p["tiles"])
             if ev: ev[i][4].record(stream)
         # L2 flush: write a buffer larger than L2, then read another one so the
         # cache holds clean lines when the decode matmuls start
@@ -255,7 +259,7 @@ def run_ours(args, rank, world):
         # inside the timed segment
         fence.zero_()
         for p in projs:
-            wb.w4a16_gemm(p["x"], p["qw"], p["sc"], p["ze"], out=p["y"])
+            wb.w4a16_gemm_repacked(p["x"], p["tiles"], p["N"], out=p["y"])
         if ev: ev[4][1].record(stream)
 
     for _ in range(args.warmup):
@@ -301,8 +305,7 @@ def run_ours(args, rank, world):
     # after an L2 flush (and the same one-element fence kernel)
     # (all repetitions are queued before any is read, so the host never
     # leaves the GPU idle inside a timed launch)
-    per_gemv = []
-    for p in projs:
+    def alone(launch):
         evs_alone = []
         for _ in range(20):
             flush_w.fill_(1.0)
@@ -310,11 +313,32 @@ def run_ours(args, rank, world):
             a, b = E(), E()
             a.record(stream)
             fence.zero_()
-            wb.w4a16_gemm(p["x"], p["qw"], p["sc"], p["ze"], out=p["y"])
+            launch()
             b.record(stream)
             evs_alone.append((a, b))
         torch.cuda.synchronize()
-        per_gemv.append(statistics.median(a.elapsed_time(b) for a, b in evs_alone))
+        return statistics.median(a.elapsed_time(b) for a, b in evs_alone)
+
+    per_gemv = [alone(lambda p=p: wb.w4a16_gemm_repacked(p["x"], p["tiles"], p["N"], out=p["y"]))
+                for p in projs]
+    per_gemv_plain = [alone(lambda p=p: wb.w4a16_gemm(p["x"], p["qw"], p["sc"], p["ze"],
+                                                      out=p["y"])) for p in projs]
+
+    # the same four-launch decode segment on the plain packed layout
+    # (w4a16_gemm), for comparison with the repacked tiles
+    seg_plain = []
+    for _ in range(20):
+        flush_w.fill_(1.0)
+        torch.sum(flush_r, dim=0, out=flush_out)
+        a, b = E(), E()
+        a.record(stream)
+        fence.zero_()
+        for p in projs:
+            wb.w4a16_gemm(p["x"], p["qw"], p["sc"], p["ze"], out=p["y"])
+        b.record(stream)
+        seg_plain.append((a, b))
+    torch.cuda.synchronize()
+    seg_plain_ms = statistics.median(a.elapsed_time(b) for a, b in seg_plain)
 
     # Size-matched read ceiling: a plain streaming read (torch.sum) of as many
     # bytes as each decode launch moves, timed the same way.  Single launches
@@ -362,9 +386,10 @@ def run_ours(args, rank, world):
                    "l2": "flushed every step before the decode matmuls (512 MiB write + 512 MiB "
                          "read); the step's fp16 weights (405 MB) also exceed L2",
                    "parallelism": f"replicas x{world} (one layer per GPU, no collective)",
-                   "value_basis": "decode-matmul algorithmic bytes / CUDA-event time of the "
-                                  "decode segment of each timed step (the four launches back "
-                                  "to back, after the L2 flush)",
+                   "value_basis": "decode-matmul algorithmic bytes (packed weights, scales, "
+                                  "zero-points, x, y) / CUDA-event time of the decode segment "
+                                  "of each timed step (the four launches back to back, after "
+                                  "the L2 flush), over the repacked decode tiles",
                    "decode_overlap": "programmatic dependent launch with early weight fetch "
                                      "(awq_set_weight_prefetch 1): consecutive decode launches "
                                      "overlap; no launch's weights are written by the kernel "
@@ -381,24 +406,28 @@ def run_ours(args, rank, world):
                                      "candidate scales) are within a few percent",
                      "timing": "CUDA events around each awq_search_scale call (includes its "
                                "candidate-scale and final-reduction kernels)"},
-        "roofline_gemv": {"kernel": "gemv_w4a16_kernel<1> (4 launches per step)", "bound": "hbm",
+        "roofline_gemv": {"kernel": "gemv_tiles_kernel<1,16> (4 launches per step)", "bound": "hbm",
                           "achieved": round(gemv_gbs, 1), "peak": peaks["hbm_gbs"],
                           "unit": "GB/s", "frac": round(gemv_gbs / peaks["hbm_gbs"], 4),
                           "peak_source": f"{peak_src} copy bandwidth",
                           "size_matched_read_gbs": round(bytes_step / (sum(read_ms) * 1e-3) / 1e9, 1),
                           "size_matched_read_note": "torch.sum over each launch's byte count, "
                                                     "one launch at a time after the L2 flush; "
-                                                    "sum of bytes / sum of times"},
+                                                    "sum of bytes / sum of times",
+                          "plain_layout_segment_gbs": round(bytes_step / (seg_plain_ms * 1e-3) / 1e9, 1),
+                          "plain_layout_note": "the same four launches with w4a16_gemm on the "
+                                               "plain packed layout, median of 20 segments"},
         "stages_ms_per_step": {k: round(v / args.steps, 4) for k, v in st.items()},
         "per_projection": {p["name"]: {"search_ms": round(per_search[i] / args.steps, 4),
                                        "gemv_us_alone": round(per_gemv[i] * 1e3, 2),
+                                       "gemv_plain_us_alone": round(per_gemv_plain[i] * 1e3, 2),
                                        "gemv_gbs_alone": round(gemv_bytes(p["N"], p["K"]) /
                                                                (per_gemv[i] * 1e-3) / 1e9, 1),
                                        "read_us_alone": round(read_ms[i] * 1e3, 2)}
                            for i, p in enumerate(projs)},
         # per projection and step: stats, mean, two candidate-scale kernels, search,
-        # finalize, pack, decode
-        "gpu_launches": args.steps * 4 * 8,
+        # finalize, pack, repack, decode
+        "gpu_launches": args.steps * 4 * 9,
         "clocks": clocks,
     }
     if not args.no_e2e:
@@ -519,6 +548,7 @@ def run_e2e(args, projs, dev, stream, world, fence):
             wb.search_scale(p["W"], p["Xc"], p["mean"], workspace=p["ws"],
                             out=(p["s"], p["mse"], p["best"]))
             wb.pack_int4(p["W"], p["s"], out=(p["qw"], p["sc"], p["ze"]))
+            wb.repack_int4(p["qw"], p["sc"], p["ze"], out=p["tiles"])
             e2 = E()
             e2.record(stream)
             done_pack.append(e2)
@@ -529,7 +559,7 @@ def run_e2e(args, projs, dev, stream, world, fence):
                     dst.copy_(src, non_blocking=True)
         fence.zero_()
         for p in projs:
-            wb.w4a16_gemm(p["x"], p["qw"], p["sc"], p["ze"], out=p["y"])
+            wb.w4a16_gemm_repacked(p["x"], p["tiles"], p["N"], out=p["y"])
         released.record(stream)
         copy_stream.wait_event(released)
         with torch.cuda.stream(copy_stream):

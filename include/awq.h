@@ -242,6 +242,48 @@ awq_status w4a16_gemm_scaled(const uint16_t* X, int64_t M, int64_t K, int64_t ld
                              void* workspace, size_t ws_bytes, awq_stream_t stream);
 size_t w4a16_gemm_scaled_workspace_size(int64_t M, int64_t N, int64_t K);
 
+/* ---- weight packing for the decode kernel: repacked tiles ------------------
+ * The OpenAlex record's abstract names weight packing for the inference
+ * kernels; the AWQ page's first paragraph: decoding is memory-bound.  The
+ * plain layout of awq_pack_int4 spreads the 16 rows a decode warp works on
+ * over the matrix; the repack gathers each (16-row slab, group of 128) into
+ * one contiguous 1088-byte tile, so the decode matmul streams contiguous
+ * bytes.  Tile (j, g) of slab j (rows 16 j .. 16 j + 15) and group g sits at
+ * byte (j * (K/128) + g) * 1088:
+ *   bytes [0, 1024): chunk c = 32 h + L (h = 0, 1; L = 0..31) of 16 bytes is
+ *     bytes 64 g + 16 (L % 4) .. +15 of row 16 j + L / 4 + 8 h of qweight
+ *     (i.e. its words 16 g + 4 (L % 4) .. +3);
+ *   bytes [1024, 1088): for r = 0..7, 8 bytes: the fp16 scale and zero-point
+ *     of row 16 j + r, then those of row 16 j + r + 8.
+ * Rows at or past N are zero.  Nothing is rounded or changed: the tiles hold
+ * the same packed words, scales and zero-points.
+ *   qweight, scales, zeros: as written by awq_pack_int4 for an [N, K] weight.
+ *   tiles    device buffer of at least awq_repack_int4_bytes(N, K) bytes,
+ *            16-byte aligned (written completely).
+ * K % 128 == 0, group == 128; qweight 16-byte aligned. */
+size_t awq_repack_int4_bytes(int64_t N, int64_t K);
+awq_status awq_repack_int4(const uint32_t* qweight, const uint16_t* scales, const uint16_t* zeros,
+                           int64_t N, int64_t K, int group, void* tiles, size_t tiles_bytes,
+                           awq_stream_t stream);
+
+/* Y = X deq(Wq)^T for 1 <= M <= 16 tokens over the repacked tiles, with the
+ * arithmetic of w4a16_gemm's decode kernel (deq = (q - z) * scale, exact fp16
+ * (q - z), fp32 accumulation per group, the group scale applied in fp32,
+ * fp16 out) and the packed bytes streamed contiguously (AWQ page, first
+ * paragraph: memory-bound decoding).  The split of K over warps depends only
+ * on N and K, so results are deterministic; they may differ from
+ * w4a16_gemm's in the last fp32 roundings (another split).
+ *   X      [M, K] fp16, leading dimension ldx (>= K, multiple of 8).
+ *   inv_s  [K] fp32 or NULL: when given, X is used as fp16(fp32(X) * inv_s)
+ *          (the fused input scaling of w4a16_gemm_scaled).
+ *   tiles  from awq_repack_int4 for an [N, K] weight; N % 8 == 0.
+ *   Y      [M, N] fp16, leading dimension ldy (>= N).
+ * M > 16 returns AWQ_ERR_SHAPE.  No workspace.  X, tiles, inv_s 16-byte
+ * aligned.  Weight prefetch follows awq_set_weight_prefetch. */
+awq_status w4a16_gemm_repacked(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
+                               const float* inv_s, const void* tiles, int64_t N, int group,
+                               uint16_t* Y, int64_t ldy, awq_stream_t stream);
+
 /* Overlap of back-to-back decode matmuls (M <= 16).  Every decode launch
  * lets the next kernel in the stream start beside it (programmatic dependent
  * launch) and reads X / writes Y only after the previous kernel in the stream

@@ -50,6 +50,10 @@ def test_version_and_workspace_sizes(capi):
     assert n >= 20 * 4096 * (4 + 4 + 8) + 20 * 96 * 4 * 8
     assert capi.awq_search_workspace_size(0, 4096, 512, 20) == 0
     assert capi.awq_candidate_scales_workspace_size(4096, 20) >= 20 * 4096 * 8
+    # decode tiles: 1088 bytes per (16-row slab, group of 128), N rounded up to 16
+    assert capi.awq_repack_int4_bytes(12288, 4096) == 768 * 32 * 1088
+    assert capi.awq_repack_int4_bytes(136, 384) == 9 * 3 * 1088
+    assert capi.awq_repack_int4_bytes(16, 100) == 0
 
 
 def test_host_argument_checks(capi):
@@ -95,6 +99,17 @@ def test_host_argument_checks(capi):
     assert capi.w3a16_gemm(base, 1, 128, 128, base, base, base, 12, 128, base, 12, None) == 2
     assert capi.w3a16_gemm(base + 2, 1, 128, 128, base, base, base, 8, 128, base, 8, None) == 3
     assert capi.w3a16_gemm(None, 1, 128, 128, base, base, base, 8, 128, base, 8, None) == 1
+    # repack: K % 128, tiles buffer too small, misaligned tiles
+    assert capi.awq_repack_int4(base, base, base, 16, 100, 128, base, 4096, None) == 2
+    assert capi.awq_repack_int4(base, base, base, 16, 128, 128, base, 1087, None) == 5
+    assert capi.awq_repack_int4(base, base, base, 16, 128, 128, base + 8, 4096, None) == 3
+    # repacked matmul: decode sizes only, N % 8, misaligned X or tiles
+    assert capi.w4a16_gemm_repacked(base, 17, 128, 128, None, base, 16, 128, base, 16, None) == 2
+    assert capi.w4a16_gemm_repacked(base, 1, 128, 128, None, base, 12, 128, base, 12, None) == 2
+    assert capi.w4a16_gemm_repacked(base + 2, 1, 128, 128, None, base, 16, 128, base, 16,
+                                    None) == 3
+    assert capi.w4a16_gemm_repacked(base, 1, 128, 128, None, base + 8, 16, 128, base, 16,
+                                    None) == 3
     assert capi.awq_last_error_string()
 
 

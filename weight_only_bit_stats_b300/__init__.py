@@ -12,6 +12,8 @@ Steps (names follow the C ABI in ``include/awq.h``):
 * ``search_scale``              -- alpha grid search by output MSE
 * ``pack_int4``                 -- asymmetric INT4, group 128, fp16 scale/zero
 * ``w4a16_gemm``                -- Y = X deq(Wq)^T, fp32 accumulate, fp16 out
+* ``repack_int4``               -- packed weights -> contiguous decode tiles
+* ``w4a16_gemm_repacked``       -- the decode matmul (M <= 16) over the tiles
 """
 from __future__ import annotations
 
@@ -22,6 +24,7 @@ import torch
 
 __all__ = ["AwqError", "lib", "act_stats", "act_mean", "candidate_scales", "search_scale",
            "pack_int4", "pack_int3", "w4a16_gemm", "w3a16_gemm", "w4a16_gemm_scaled",
+           "repack_int4", "w4a16_gemm_repacked",
            "set_weight_prefetch",
            "sync_status",
            "ALPHA_GRID",
@@ -67,6 +70,9 @@ SIGNATURES = (
     ("w4a16_gemm_scaled", _int, [_p, _i64, _i64, _i64, _p, _p, _p, _p, _i64, _int, _p, _i64, _p,
                                  _sz, _p]),
     ("w4a16_gemm_scaled_workspace_size", _sz, [_i64, _i64, _i64]),
+    ("awq_repack_int4_bytes", _sz, [_i64, _i64]),
+    ("awq_repack_int4", _int, [_p, _p, _p, _i64, _i64, _int, _p, _sz, _p]),
+    ("w4a16_gemm_repacked", _int, [_p, _i64, _i64, _i64, _p, _p, _i64, _int, _p, _i64, _p]),
     ("awq_set_weight_prefetch", _int, [_int]),
     ("awq_selftest_wait_timeout", _int, [_i64, _p]),
     ("awq_sync_status", _int, [_p]),
@@ -268,6 +274,44 @@ def w4a16_gemm(X: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, zer
                             zeros.data_ptr(), N, GROUP, Y.data_ptr(), _ld(Y),
                             ws.data_ptr() if ws is not None else None, ws_n, _stream(stream)),
            "w4a16_gemm")
+    return Y
+
+
+def repack_int4(qweight: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The packed weights regrouped into contiguous decode tiles (uint8
+    [awq_repack_int4_bytes(N, K)]), one 1088-byte tile per 16 rows x 128
+    input channels."""
+    _dev(qweight, torch.int32, "qweight")
+    _dev(scales, torch.float16, "scales")
+    _dev(zeros, torch.float16, "zeros")
+    N, K8 = qweight.shape
+    K = K8 * 8
+    nbytes = lib().awq_repack_int4_bytes(N, K)
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=qweight.device)
+    _dev(out, torch.uint8, "tiles")
+    _check(lib().awq_repack_int4(qweight.data_ptr(), scales.data_ptr(), zeros.data_ptr(), N, K,
+                                 GROUP, out.data_ptr(), out.numel(), _stream(stream)),
+           "awq_repack_int4")
+    return out
+
+
+def w4a16_gemm_repacked(X: torch.Tensor, tiles: torch.Tensor, N: int,
+                        inv_s: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """Y = X deq(Wq)^T over the decode tiles of an [N, K] weight, M <= 16;
+    with ``inv_s`` the input is fp16(X * inv_s)."""
+    _dev(X, torch.float16, "X")
+    _dev(tiles, torch.uint8, "tiles")
+    if inv_s is not None:
+        _dev(inv_s, torch.float32, "inv_s")
+    M, K = X.shape
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=X.device)
+    _check(lib().w4a16_gemm_repacked(X.data_ptr(), M, K, _ld(X),
+                                     inv_s.data_ptr() if inv_s is not None else None,
+                                     tiles.data_ptr(), N, GROUP, Y.data_ptr(), _ld(Y),
+                                     _stream(stream)), "w4a16_gemm_repacked")
     return Y
 
 

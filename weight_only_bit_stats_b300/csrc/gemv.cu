@@ -37,12 +37,13 @@
 //    The work split depends on N and K only, so the result is deterministic
 //    and independent of M, and the kernel needs no workspace.
 #include "common.cuh"
+#include "decode.cuh"
 #include "kernels.cuh"
 
 namespace awq {
 namespace {
 
-constexpr int kDecRows = 16;                        // rows per slab (MMA M)
+using namespace dec;
 // Groups per ring stage.  One TMA box per stage: 16 rows x kDecChunk groups
 // (row pitch kDecChunk * 64 B in shared memory).  An odd count makes the
 // pitch an odd multiple of 64 B, so the two rows a quarter warp reads sit on
@@ -73,79 +74,6 @@ constexpr size_t kDecSmemMax = 232448;                 // per-block opt-in limit
 static_assert(DecCfg<1>::kSmem <= kDecSmemMax && DecCfg<2>::kSmem <= kDecSmemMax,
               "decode kernel exceeds shared memory");
 
-// Shared-memory activations: per token a row of G * 256 + 64 bytes; within
-// a group, the 8-element chunk of physical k = 32 t + 8 i sits at chunk
-// position 4 i + t already in fragment order (x0,x4)(x1,x5)(x2,x6)(x3,x7).
-// The 64-byte pad puts consecutive tokens on different bank halves.
-__host__ __device__ constexpr int64_t dec_x_row_bytes(int64_t G) { return G * 256 + 64; }
-
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
-__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
-
-// One 32-bit word (8 nibbles n0..n7, n_i at bits 4i) -> four fp16x2 pairs
-// (n0,n4) (n1,n5) (n2,n6) (n3,n7), each minus the zero-point, exact.
-__device__ __forceinline__ void dequant_word(uint32_t w, __half2 z1024, __half2 zneg64,
-                                             uint32_t (&p)[4]) {
-    const uint32_t magic = 0x64006400u;               // fp16x2 (1024, 1024)
-    const __half2 sixteenth = __half2half2(__float2half_rn(0.0625f));
-    uint32_t v0 = lop3_and_or(w, 0x000F000Fu, magic);        // 1024 + n0 | 1024 + n4
-    uint32_t v1 = lop3_and_or(w, 0x00F000F0u, magic);        // 1024 + 16 n1 | ...
-    uint32_t w8 = w >> 8;
-    uint32_t v2 = lop3_and_or(w8, 0x000F000Fu, magic);       // n2 | n6
-    uint32_t v3 = lop3_and_or(w8, 0x00F000F0u, magic);       // 16 n3 | 16 n7
-    p[0] = h2_as_u32(__hsub2(u32_as_h2(v0), z1024));
-    p[1] = h2_as_u32(__hfma2(u32_as_h2(v1), sixteenth, zneg64));
-    p[2] = h2_as_u32(__hsub2(u32_as_h2(v2), z1024));
-    p[3] = h2_as_u32(__hfma2(u32_as_h2(v3), sixteenth, zneg64));
-}
-
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// x * inv_s for 8 consecutive activations: fp32 product, rounded once to
-// fp32 and once to fp16 (the fused form of the caller's "divide by s").
-__device__ __forceinline__ uint4 scale_x8(uint4 v, const float* inv_s) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(inv_s));
-    const float4 b = __ldg(reinterpret_cast<const float4*>(inv_s) + 1);
-    const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const __half2 h = *reinterpret_cast<const __half2*>(&w[j]);
-        const __half2 r = __floats2half2_rn(__fmul_rn(__low2float(h), f[2 * j]),
-                                            __fmul_rn(__high2float(h), f[2 * j + 1]));
-        w[j] = *reinterpret_cast<const uint32_t*>(&r);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// 8 physical activations (x0..x7) -> the B-fragment order of the permuted k:
-// (x0,x4) (x1,x5) (x2,x6) (x3,x7).
-__device__ __forceinline__ uint4 permute_x8(uint4 v) {
-    uint4 o;
-    o.x = prmt(v.x, v.z, 0x5410);
-    o.y = prmt(v.x, v.z, 0x7632);
-    o.z = prmt(v.y, v.w, 0x5410);
-    o.w = prmt(v.y, v.w, 0x7632);
-    return o;
-}
-
 // Scale and zero-point of a thread's two rows for the groups of one chunk,
 // loaded one chunk ahead.
 struct ChunkSZ {
@@ -168,90 +96,6 @@ __device__ __forceinline__ void load_chunk_sz(ChunkSZ& z, const GemvParams& p, i
         z.sb[j] = (vb && in) ? __ldg(sb + gi) : (uint16_t)0;
         z.zb[j] = (vb && in) ? __ldg(zb + gi) : (uint16_t)0;
     }
-}
-
-// A thread's 64 bytes of each token's activations for one group, in
-// fragment order (used when the activations are not staged in shared memory).
-template <int NB>
-struct GroupX {
-    uint4 x[NB][4];
-};
-
-template <int NB>
-__device__ __forceinline__ void load_group_x(GroupX<NB>& in, const GemvParams& p, int gi, int g,
-                                             int t) {
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-        // lanes of absent tokens read the last token (their column is dropped)
-        const int tok = min(g + 8 * nb, p.M - 1);
-        const uint4* xp = reinterpret_cast<const uint4*>(p.X + (int64_t)tok * p.ldx +
-                                                         (int64_t)gi * kGroup + 32 * t);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint4 v = __ldg(xp + i);
-            if (p.inv_s) v = scale_x8(v, p.inv_s + (int64_t)gi * kGroup + 32 * t + 8 * i);
-            in.x[nb][i] = permute_x8(v);
-        }
-    }
-}
-
-// y += scale * (X_group (q - z)^T) for one group: 8 (16 for NB = 2) MMAs in
-// two independent accumulator chains, added in a fixed order.  xs: this
-// thread's staged activation rows (XS), one per n-tile, or null for a token
-// beyond M.
-template <int NB, bool XS>
-__device__ __forceinline__ void group_mma(float (&y)[NB][4], uint16_t sa16, uint16_t sb16,
-                                          uint16_t za16, uint16_t zb16, const GroupX<NB>& gx,
-                                          uint4 wa, uint4 wb, const uint8_t* const (&xs)[NB],
-                                          int gi, int t) {
-    const __half za = __ushort_as_half(za16), zb = __ushort_as_half(zb16);
-    const __half h1024 = __float2half_rn(1024.0f), h64 = __float2half_rn(64.0f);
-    const __half2 za1024 = __half2half2(__hadd(h1024, za));
-    const __half2 zb1024 = __half2half2(__hadd(h1024, zb));
-    const __half2 zaneg = __half2half2(__hneg(__hadd(h64, za)));
-    const __half2 zbneg = __half2half2(__hneg(__hadd(h64, zb)));
-    const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
-    const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
-    float c[NB][2][4];
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) c[nb][i][j] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint32_t pa[4], pb[4];
-        dequant_word(wA[i], za1024, zaneg, pa);
-        dequant_word(wB[i], zb1024, zbneg, pb);
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-            uint4 b;
-            if constexpr (XS) {
-                b = *reinterpret_cast<const uint4*>(xs[nb] + gi * 256 + (i * 4 + t) * 16);
-            } else {
-                b = gx.x[nb][i];
-            }
-            mma16816(c[nb][i & 1], pa[0], pb[0], pa[1], pb[1], b.x, b.y);
-            mma16816(c[nb][i & 1], pa[2], pb[2], pa[3], pb[3], b.z, b.w);
-        }
-    }
-    const float fsa = __half2float(__ushort_as_half(sa16));
-    const float fsb = __half2float(__ushort_as_half(sb16));
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-        y[nb][0] = fmaf(fsa, c[nb][0][0] + c[nb][1][0], y[nb][0]);
-        y[nb][1] = fmaf(fsa, c[nb][0][1] + c[nb][1][1], y[nb][1]);
-        y[nb][2] = fmaf(fsb, c[nb][0][2] + c[nb][1][2], y[nb][2]);
-        y[nb][3] = fmaf(fsb, c[nb][0][3] + c[nb][1][3], y[nb][3]);
-    }
-}
-
-// First unit of warp j when U units are split over NW warps (division by a
-// compile-time constant).
-template <int NW>
-__device__ __forceinline__ int warp_lo(int U, int j) {
-    return (int)(((int64_t)j * U) / NW);
 }
 
 template <int NW>
@@ -338,17 +182,7 @@ __global__ void __launch_bounds__(NW * 32, DecCfg<NB>::kMinBlocks)
     const uint8_t* xs[NB];
     if constexpr (XS) {
         const int64_t xrow = dec_x_row_bytes(p.G);
-        const int chunks = p.M * p.G * 16;
-        for (int cix = threadIdx.x; cix < chunks; cix += kDecThreads) {
-            const int m = cix / (p.G * 16), rem = cix - m * p.G * 16;
-            const int gl = rem >> 4, k8 = rem & 15;
-            uint4 v = __ldg(reinterpret_cast<const uint4*>(
-                p.X + (int64_t)m * p.ldx + (int64_t)gl * kGroup + k8 * 8));
-            if (p.inv_s) v = scale_x8(v, p.inv_s + (int64_t)gl * kGroup + k8 * 8);
-            const int tt = k8 >> 2, ii = k8 & 3;
-            *reinterpret_cast<uint4*>(xsm + m * xrow + gl * 256 + (ii * 4 + tt) * 16) =
-                permute_x8(v);
-        }
+        stage_x(xsm, p.X, p.ldx, p.M, p.inv_s, p.G, threadIdx.x, kDecThreads);
         __syncthreads();
         // an MMA output column depends only on its own B column, so lanes of
         // absent tokens read the last token's row and their outputs are dropped
@@ -419,7 +253,7 @@ __global__ void __launch_bounds__(NW * 32, DecCfg<NB>::kMinBlocks)
         ChunkSZ nsz;
         if (i + 1 < n_my) load_chunk_sz(nsz, p, (int64_t)(s0 + nsl) * kDecRows + g, nch * kDecChunk);
         GroupX<NB> gx;
-        if constexpr (!XS) load_group_x<NB>(gx, p, gb, g, t);
+        if constexpr (!XS) load_group_x<NB>(gx, p.X, p.ldx, p.M, p.inv_s, gb, g, t);
         const int s = i % kDecStages;
         if (!mbar_wait(&ctl->full[warp][s], (uint32_t)(i / kDecStages) & 1u, &ctl->abort,
                        p.status)) {
@@ -434,7 +268,7 @@ __global__ void __launch_bounds__(NW * 32, DecCfg<NB>::kMinBlocks)
                 GroupX<NB> cx;
                 if constexpr (!XS) {
                     cx = gx;
-                    if (gi + 1 < ge) load_group_x<NB>(gx, p, gi + 1, g, t);
+                    if (gi + 1 < ge) load_group_x<NB>(gx, p.X, p.ldx, p.M, p.inv_s, gi + 1, g, t);
                 }
                 const uint8_t* gbox = box + jg * 64 + t * 16;
                 const uint4 wa = *reinterpret_cast<const uint4*>(gbox + g * kDecPitch);

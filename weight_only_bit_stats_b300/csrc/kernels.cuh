@@ -58,6 +58,27 @@ struct GemvParams {
 cudaError_t launch_gemv(const CUtensorMap& mapW, const GemvParams& p, int num_sms,
                         cudaStream_t st);
 
+// ---- decode matmul over the repacked decode tiles, and the repack
+// (gemv_tiles.cu) ----
+constexpr int kTileBytes = 1088;   // one (16-row slab, group of 128) tile
+struct TileParams {
+    const uint16_t* X;
+    int64_t ldx;
+    int M;
+    const uint8_t* tiles;   // ceil(N / 16) * G tiles of kTileBytes
+    int64_t N;
+    int G;
+    uint16_t* Y;
+    int64_t ldy;
+    unsigned* status;
+    int early_weights;   // 1: weights may be fetched before the previous kernel completes
+    const float* inv_s;  // [K] or null: X is used as fp16(X * inv_s)
+};
+cudaError_t launch_gemv_tiles(const TileParams& p, int num_sms, cudaStream_t st);
+cudaError_t launch_repack_int4(const uint32_t* qweight, const uint16_t* scales,
+                               const uint16_t* zeros, int64_t N, int64_t K, void* tiles,
+                               int num_sms, cudaStream_t st);
+
 // ---- tensor-core kernels (tc.cu): W4A16 GEMM and the alpha search ----
 struct TcParams {
     int N, K, G;

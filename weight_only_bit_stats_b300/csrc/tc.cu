@@ -375,13 +375,16 @@ __device__ void role_prod_gemm(const TcParams& p, uint8_t* As, SmemCtl* ctl, int
 }
 
 // ---- role: search producer (fake-quantise W diag(s), residual E in fp16) ----
-// Eight lanes hold one row of the group: lane c the channels 8c..8c+7 and
-// 64+8c..64+8c+7 (one 16-byte chunk in each 64-channel sub-tile, so the
-// eight lanes of a row fill 128 contiguous swizzled bytes per store).  A
-// warp covers 4 rows per pass, 16 warps x 2 passes the 128-row tile.  The
-// levels are the packer's (same rounding points), computed with the fast
+// Four lanes hold one row of the group: lane c the 16-byte chunks c and c + 4
+// of both 64-channel sub-tiles (channels 8c..8c+7, 32+8c.., 64+8c..,
+// 96+8c..), 32 channels in all, so the group's range takes two shuffle
+// rounds and each lane forms the group parameters once per 32 elements.  A
+// warp covers 8 rows, the 16 producer warps the 128-row tile in one pass.
+// The levels are the packer's (same rounding points), computed with the fast
 // exact quotient; E = (q - z) scale / s - W is formed as
-// ((q - z) scale - w') (1/s) in fp32 and rounded once to fp16.
+// ((q - z) scale - w') (1/s): the FFMA rounds (q - z) scale - w' once, and
+// (q - z) scale is exact (at most 4 + 11 significant bits), so this is the
+// value of one fp32 subtraction; times 1/s and rounded to fp16.
 __device__ __forceinline__ void unpack8(uint4 v, float4 sa, float4 sb, float* wp) {
     const __half2* h = reinterpret_cast<const __half2*>(&v);
     const float2 f0 = __half22float2(h[0]), f1 = __half22float2(h[1]);
@@ -403,79 +406,80 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 
 template <int PW>
 __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, int pw, int lane) {
-    static_assert(PW * 4 * 2 == kTcRows, "16 producer warps x 4 rows x 2 passes");
+    static_assert(PW * 8 == kTcRows, "16 producer warps x 8 rows");
     volatile int* abort = &ctl->abort;
-    const int rr = lane >> 3, c = lane & 7;
+    const int rr = lane >> 2, c = lane & 3;
+    const int r = pw * 8 + rr;                          // this lane's row of the tile
+    // the lane's four chunks q: sub-tile q / 2, chunk c + 4 (q % 2) (k = 64 (q / 2) + 8 c
+    // + 32 (q % 2)); within a sub-tile the two chunks sit 64 bytes apart after the
+    // swizzle (chunk index XOR row % 8 flips only its low three bits)
+    const uint32_t soff0 = sw128_offset(r, 8 * c);
     uint32_t a_iter = 0;
     bool bad = false;
     for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
         const Item it = decode_item<kModeSearch>(item, p);
         const float* s_a = p.s_alpha + (int64_t)it.alpha * p.K;
         const float* is_a = p.inv_s_alpha + (int64_t)it.alpha * p.K;
+        const int64_t n = (int64_t)it.n_tile * kTcRows + r;
+        const bool valid = n < p.N;
+        const uint16_t* wrow = p.W + (valid ? n : 0) * p.ldw;
         for (int g = 0; g < p.G; ++g) {
-            const int64_t k0 = (int64_t)g * kGroup + 8 * c;
-            uint4 raw[2][2];
+            const int64_t kg = (int64_t)g * kGroup;
+            uint4 raw[4];
 #pragma unroll
-            for (int ps = 0; ps < 2; ++ps) {
-                const int64_t n = (int64_t)it.n_tile * kTcRows + ps * 64 + pw * 4 + rr;
-                if (n < p.N) {
-                    const uint16_t* wr = p.W + n * p.ldw + k0;
-                    raw[ps][0] = __ldg(reinterpret_cast<const uint4*>(wr));
-                    raw[ps][1] = __ldg(reinterpret_cast<const uint4*>(wr + 64));
-                } else {
-                    raw[ps][0] = raw[ps][1] = make_uint4(0, 0, 0, 0);
-                }
+            for (int q = 0; q < 4; ++q) {
+                const int k = 64 * (q >> 1) + 8 * (c + 4 * (q & 1));
+                raw[q] = valid ? __ldg(reinterpret_cast<const uint4*>(wrow + kg + k))
+                               : make_uint4(0, 0, 0, 0);
             }
+            // phase 1: w' = fp32(W s) for the 32 channels, and their range
+            float wp[32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int k = 64 * (q >> 1) + 8 * (c + 4 * (q & 1));
+                const float4* sp = reinterpret_cast<const float4*>(s_a + kg + k);
+                unpack8(raw[q], __ldg(sp), __ldg(sp + 1), wp + 8 * q);
+            }
+            float lo = fmin3_nan(wp[0], wp[1], wp[2]), hi = fmax3_nan(wp[0], wp[1], wp[2]);
+#pragma unroll
+            for (int e = 3; e < 31; e += 2) {
+                lo = fmin3_nan(lo, wp[e], wp[e + 1]);
+                hi = fmax3_nan(hi, wp[e], wp[e + 1]);
+            }
+            lo = fmin_nan(lo, wp[31]);
+            hi = fmax_nan(hi, wp[31]);
+            // this lane's 32 values: NaN or Inf makes lo or hi non-finite
+            bad |= !(isfinite(lo) && isfinite(hi));
+#pragma unroll
+            for (int o = 1; o < 4; o <<= 1) {
+                lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+                hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+            }
+            const GroupQuant gq = group_quant_from_range(lo, hi);
+            bad |= !gq.finite;
+            const float neg_z = -gq.zf, top_z = 15.0f - gq.zf;
             const int st = a_iter % kNA;
             if (!mbar_wait(&ctl->a_empty[st], ((a_iter / kNA) & 1u) ^ 1u, abort, p.status)) return;
             uint8_t* tile = As + st * kAStage;
+            // phase 2: levels, residual, fp16, one 16-byte store per chunk
 #pragma unroll
-            for (int ps = 0; ps < 2; ++ps) {
-                const int r = ps * 64 + pw * 4 + rr;
-                float wp[16];
-                {   // s is the same for every row: L1-resident, reloaded per pass
-                    const float4* sp = reinterpret_cast<const float4*>(s_a + k0);
-                    unpack8(raw[ps][0], __ldg(sp), __ldg(sp + 1), wp);
-                    unpack8(raw[ps][1], __ldg(sp + 16), __ldg(sp + 17), wp + 8);
+            for (int q = 0; q < 4; ++q) {
+                const int k = 64 * (q >> 1) + 8 * (c + 4 * (q & 1));
+                const float4 i0 = __ldg(reinterpret_cast<const float4*>(is_a + kg + k));
+                const float4 i1 = __ldg(reinterpret_cast<const float4*>(is_a + kg + k + 4));
+                const float is[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
+                float e[8];
+                rint_quot8(wp + 8 * q, gq.scale, gq.rcp, e);
+                uint32_t o[4];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float qz = fminf(fmaxf(e[j], neg_z), top_z);     // (q - z)
+                    e[j] = __fmul_rn(__fmaf_rn(qz, gq.scale, -wp[8 * q + j]), is[j]);
                 }
-                float lo = wp[0], hi = wp[0];
 #pragma unroll
-                for (int e = 1; e < 16; ++e) {
-                    lo = fmin_nan(lo, wp[e]);
-                    hi = fmax_nan(hi, wp[e]);
-                }
-                // this lane's 16 values: NaN or Inf makes lo or hi non-finite
-                const bool lane_bad = !(isfinite(lo) && isfinite(hi));
-#pragma unroll
-                for (int o = 1; o < 8; o <<= 1) {
-                    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-                    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-                }
-                bad |= lane_bad;
-                const GroupQuant gq = group_quant_from_range(lo, hi);
-                bad |= !gq.finite;
-                const float neg_z = -gq.zf, top_z = 15.0f - gq.zf;
-                uint32_t o[8];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const float4 i0 = __ldg(reinterpret_cast<const float4*>(is_a + k0 + 64 * h));
-                    const float4 i1 = __ldg(reinterpret_cast<const float4*>(is_a + k0 + 64 * h + 4));
-                    const float is[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
-                    float e[8];
-                    rint_quot8(wp + 8 * h, gq.scale, gq.rcp, e);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float w = wp[8 * h + j];
-                        const float qz = fminf(fmaxf(e[j], neg_z), top_z);    // (q - z)
-                        e[j] = __fmul_rn(__fsub_rn(__fmul_rn(qz, gq.scale), w), is[j]);
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) o[4 * h + j] = pack_h2(e[2 * j], e[2 * j + 1]);
-                }
-                *reinterpret_cast<uint4*>(tile + sw128_offset(r, 8 * c)) =
-                    make_uint4(o[0], o[1], o[2], o[3]);
-                *reinterpret_cast<uint4*>(tile + kASub + sw128_offset(r, 8 * c)) =
-                    make_uint4(o[4], o[5], o[6], o[7]);
+                for (int j = 0; j < 4; ++j) o[j] = pack_h2(e[2 * j], e[2 * j + 1]);
+                const uint32_t off = (uint32_t)((q >> 1) * kASub) + ((q & 1) ? (soff0 ^ 64u) : soff0);
+                *reinterpret_cast<uint4*>(tile + off) = make_uint4(o[0], o[1], o[2], o[3]);
             }
             fence_proxy_async_smem();
             __syncwarp();
