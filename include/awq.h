@@ -131,6 +131,40 @@ awq_status awq_search_scale(const uint16_t* W, int64_t N, int64_t K, int64_t ldw
                             awq_stream_t stream);
 size_t awq_search_workspace_size(int64_t N, int64_t K, int64_t T, int n_alpha);
 
+/* ---- alpha search through the Gram matrix ---------------------------------
+ * The pages' "quick grid search on a small calibration set" (third paragraph)
+ * fixes the objective, not how it is evaluated.  ||Xcal E^T||_F^2 =
+ * tr(E G E^T) with G = Xcal^T Xcal, so once G is formed the per-alpha cost is
+ * 2 N K^2 flops instead of 2 T N K: cheaper whenever T > K (a full
+ * calibration set of 128 x 512 tokens).
+ *
+ * awq_gram: G/T = Xcal^T Xcal / T as fp16 [K, K] (row-major, symmetric).
+ * Each element is the fp32 tensor-core sum over the T tokens, times fp32(1/T),
+ * rounded once to fp16.
+ *   Xcal  [T, K] fp16, leading dimension ldx (>= K, multiple of 8).
+ *   G     [K, K] fp16 out, 16-byte aligned.
+ *   workspace >= awq_gram_workspace_size(T, K) bytes (a transposed copy of
+ *   Xcal).  K % 128 == 0, T >= 1. */
+size_t awq_gram_workspace_size(int64_t T, int64_t K);
+awq_status awq_gram(const uint16_t* Xcal, int64_t T, int64_t K, int64_t ldx, uint16_t* G,
+                    void* workspace, size_t ws_bytes, awq_stream_t stream);
+
+/* awq_search_scale_gram: the alpha search of awq_search_scale with the
+ * objective evaluated as
+ *   mse(alpha) = sum_n (E G/T E^T)_nn / N,
+ * E the same fp16 residual the direct search forms (the packer's levels);
+ * the tensor cores form E (G/T) with fp32 accumulation, and each accumulator
+ * column is multiplied by the matching residual column and summed (fp32 per
+ * 32 columns, fp64 across them).  Arguments as awq_search_scale, with G from
+ * awq_gram in place of the calibration tokens; workspace >=
+ * awq_search_gram_workspace_size(N, K, n_alpha) bytes. */
+size_t awq_search_gram_workspace_size(int64_t N, int64_t K, int n_alpha);
+awq_status awq_search_scale_gram(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                                 const uint16_t* G, const double* mean_abs, const double* alphas,
+                                 int n_alpha, int group, float* s_out, double* mse_out,
+                                 int32_t* best_idx, float* s_alpha_out, void* workspace,
+                                 size_t ws_bytes, awq_stream_t stream);
+
 /* ---- alpha search without any device allocation ---------------------------
  * No counterpart on the AWQ pages: an allocation-free variant of
  * awq_search_scale for callers that cannot allocate device memory (plug-ins

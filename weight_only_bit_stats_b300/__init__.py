@@ -10,6 +10,7 @@ Steps (names follow the C ABI in ``include/awq.h``):
 * ``act_stats`` / ``act_mean``  -- per-input-channel mean |x| (exact sums)
 * ``candidate_scales``          -- s = mean|x|^alpha, normalised
 * ``search_scale``              -- alpha grid search by output MSE
+* ``gram`` / ``search_scale_gram`` -- the same search through G/T = X^T X / T
 * ``pack_int4``                 -- asymmetric INT4, group 128, fp16 scale/zero
 * ``w4a16_gemm``                -- Y = X deq(Wq)^T, fp32 accumulate, fp16 out
 * ``repack_int4``               -- packed weights -> contiguous decode tiles
@@ -24,7 +25,7 @@ import torch
 
 __all__ = ["AwqError", "lib", "act_stats", "act_mean", "candidate_scales", "search_scale",
            "pack_int4", "pack_int3", "w4a16_gemm", "w3a16_gemm", "w4a16_gemm_scaled",
-           "repack_int4", "w4a16_gemm_repacked",
+           "repack_int4", "w4a16_gemm_repacked", "gram", "search_scale_gram",
            "set_weight_prefetch",
            "sync_status",
            "ALPHA_GRID",
@@ -71,6 +72,11 @@ SIGNATURES = (
                                  _sz, _p]),
     ("w4a16_gemm_scaled_workspace_size", _sz, [_i64, _i64, _i64]),
     ("awq_repack_int4_bytes", _sz, [_i64, _i64]),
+    ("awq_gram_workspace_size", _sz, [_i64, _i64]),
+    ("awq_gram", _int, [_p, _i64, _i64, _i64, _p, _p, _sz, _p]),
+    ("awq_search_gram_workspace_size", _sz, [_i64, _i64, _int]),
+    ("awq_search_scale_gram", _int, [_p, _i64, _i64, _i64, _p, _p, _p, _int, _int, _p, _p, _p, _p,
+                                     _p, _sz, _p]),
     ("awq_repack_int4", _int, [_p, _p, _p, _i64, _i64, _int, _p, _sz, _p]),
     ("w4a16_gemm_repacked", _int, [_p, _i64, _i64, _i64, _p, _p, _i64, _int, _p, _i64, _p]),
     ("awq_set_weight_prefetch", _int, [_int]),
@@ -173,6 +179,50 @@ def candidate_scales(mean_abs: torch.Tensor, alphas=ALPHA_GRID, stream=None) -> 
 def search_workspace(N: int, K: int, T: int, n_alpha: int, device) -> torch.Tensor:
     n = lib().awq_search_workspace_size(N, K, T, n_alpha)
     return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def gram(Xcal: torch.Tensor, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+         stream=None) -> torch.Tensor:
+    """G/T = Xcal^T Xcal / T as fp16 [K, K]."""
+    _dev(Xcal, torch.float16, "Xcal")
+    T, K = Xcal.shape
+    if out is None:
+        out = torch.empty((K, K), dtype=torch.float16, device=Xcal.device)
+    _dev(out, torch.float16, "G")
+    n = lib().awq_gram_workspace_size(T, K)
+    if workspace is None:
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=Xcal.device)
+    _check(lib().awq_gram(Xcal.data_ptr(), T, K, _ld(Xcal), out.data_ptr(), workspace.data_ptr(),
+                          workspace.numel(), _stream(stream)), "awq_gram")
+    return out
+
+
+def search_scale_gram(W: torch.Tensor, G: torch.Tensor, mean_abs: torch.Tensor,
+                      alphas=ALPHA_GRID, workspace: torch.Tensor | None = None,
+                      return_candidates: bool = False, out=None, stream=None):
+    """The alpha search through G/T from ``gram``: returns (s, mse, best)
+    like ``search_scale`` (and the candidate scales when asked)."""
+    _dev(W, torch.float16, "W")
+    _dev(G, torch.float16, "G")
+    _dev(mean_abs, torch.float64, "mean_abs")
+    N, K = W.shape
+    arr, na = _alphas(alphas)
+    if out is None:
+        s = torch.empty(K, dtype=torch.float32, device=W.device)
+        mse = torch.empty(na, dtype=torch.float64, device=W.device)
+        best = torch.empty(1, dtype=torch.int32, device=W.device)
+    else:
+        s, mse, best = out
+    cand = torch.empty((na, K), dtype=torch.float32, device=W.device) if return_candidates else None
+    n = lib().awq_search_gram_workspace_size(N, K, na)
+    if workspace is None:
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=W.device)
+    _check(lib().awq_search_scale_gram(W.data_ptr(), N, K, _ld(W), G.data_ptr(), mean_abs.data_ptr(),
+                                       arr, na, GROUP, s.data_ptr(), mse.data_ptr(), best.data_ptr(),
+                                       cand.data_ptr() if cand is not None else None,
+                                       workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "awq_search_scale_gram")
+    return (s, mse, best, cand) if return_candidates else (s, mse, best)
 
 
 def search_scale(W: torch.Tensor, Xcal: torch.Tensor, mean_abs: torch.Tensor, alphas=ALPHA_GRID,

@@ -23,7 +23,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libawq_b300.so")
 SOURCES = ["capi.cu", "stats.cu", "quant.cu", "gemv.cu", "gemv_tiles.cu", "gemv3.cu", "tc.cu",
-           "search_noalloc.cu"]
+           "gram.cu", "search_noalloc.cu"]
 HEADERS = ["common.cuh", "kernels.cuh", "int3.cuh", "decode.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",

@@ -123,10 +123,57 @@ awq_status make_act_map(CUtensorMap* map, const uint16_t* X, int64_t rows, int64
     return AWQ_OK;
 }
 
+// fp16 [rows, K] with boxes of 64 k x box_rows rows, 128-byte swizzle.
+awq_status make_map_rows(CUtensorMap* map, const uint16_t* X, int64_t rows, int64_t K, int64_t ld,
+                         int box_rows) {
+    if (!load_encoder()) return fail(AWQ_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(X), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(AWQ_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    return AWQ_OK;
+}
+
 // Packed weights [N, K/8] uint32 for the decode kernel: unswizzled boxes of
 // 48 words (three groups of 128 nibbles) x 16 rows, landing as
-// [16 rows][192 B].
+// [16 rows][192 B].  A decode step calls the same few weights over and over,
+// so the encoded maps are kept in a small per-thread cache keyed on
+// (address, N, K) -- a map holds nothing else -- and the encode (driver work
+// on the launch path) runs once per weight.
+struct QwMapEntry {
+    const uint32_t* qw = nullptr;
+    int64_t N = 0, K = 0;
+    CUtensorMap map;
+};
+constexpr int kQwMapCache = 16;
+thread_local QwMapEntry t_qw_maps[kQwMapCache];
+thread_local int t_qw_next = 0;
+
+awq_status encode_qweight_map(CUtensorMap* map, const uint32_t* qw, int64_t N, int64_t K);
+
 awq_status make_qweight_map(CUtensorMap* map, const uint32_t* qw, int64_t N, int64_t K) {
+    for (const QwMapEntry& e : t_qw_maps)
+        if (e.qw == qw && e.N == N && e.K == K) {
+            *map = e.map;
+            return AWQ_OK;
+        }
+    awq_status s = encode_qweight_map(map, qw, N, K);
+    if (s) return s;
+    QwMapEntry& e = t_qw_maps[t_qw_next];
+    t_qw_next = (t_qw_next + 1) % kQwMapCache;
+    e.qw = qw;
+    e.N = N;
+    e.K = K;
+    e.map = *map;
+    return AWQ_OK;
+}
+
+awq_status encode_qweight_map(CUtensorMap* map, const uint32_t* qw, int64_t N, int64_t K) {
     if (!load_encoder()) return fail(AWQ_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
     cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)N};
     cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
@@ -363,6 +410,123 @@ awq_status awq_search_scale(const uint16_t* W, int64_t N, int64_t K, int64_t ldw
     e = awq::launch_tc_search(map, p, d->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e);
     e = awq::launch_search_finalize(partials, n_alpha, (int64_t)p.n_tiles * p.t_tiles * 4, T, N, K,
+                                    s_alpha, mse, best_idx, s_out, st);
+    return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
+}
+
+// Tokens of the transposed copy: T rounded up to a whole 64-token TMA box.
+static int64_t gram_t_pad(int64_t T) { return (T + 63) / 64 * 64; }
+
+size_t awq_gram_workspace_size(int64_t T, int64_t K) {
+    if (T <= 0 || K <= 0) return 0;
+    return align256((size_t)K * (size_t)gram_t_pad(T) * 2);
+}
+
+awq_status awq_gram(const uint16_t* Xcal, int64_t T, int64_t K, int64_t ldx, uint16_t* G,
+                    void* workspace, size_t ws_bytes, awq_stream_t stream) {
+    const CallRange range("awq_gram");
+    if (T <= 0 || K <= 0) return fail(AWQ_ERR_INVALID_ARG, "gram: sizes must be positive");
+    if (!Xcal || !G) return fail(AWQ_ERR_INVALID_ARG, "gram: null pointer");
+    if (K % AWQ_GROUP || ldx < K || ldx % 8)
+        return fail(AWQ_ERR_SHAPE, "gram: need K % 128 == 0, ldx >= K, ldx % 8 == 0");
+    if (T > (1LL << 30) || K > (1LL << 22))
+        return fail(AWQ_ERR_SHAPE, "gram: size too large");
+    if (!aligned16(Xcal) || !aligned16(G))
+        return fail(AWQ_ERR_ALIGN, "gram: Xcal and G must be 16-byte aligned");
+    const size_t need = awq_gram_workspace_size(T, K);
+    if (!workspace || ws_bytes < need || !aligned16(workspace))
+        return fail(AWQ_ERR_WORKSPACE, "gram: workspace missing or too small");
+    DevInfo* d = nullptr;
+    awq_status s = device_info(&d);
+    if (s) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int64_t T_pad = gram_t_pad(T);
+    uint16_t* Xt = static_cast<uint16_t*>(workspace);
+    cudaError_t e = awq::launch_transpose_x(Xcal, T, K, ldx, Xt, T_pad, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    // X^T [K][T_pad]: B boxes of 64 tokens x 256 rows, A boxes of 64 x 128
+    CUtensorMap mapB, mapA;
+    s = make_act_map(&mapB, Xt, K, T_pad, T_pad);
+    if (s) return s;
+    s = make_map_rows(&mapA, Xt, K, T_pad, T_pad, awq::kTcRows);
+    if (s) return s;
+    awq::TcParams p = {};
+    p.N = (int)K;
+    p.K = (int)T_pad;
+    p.G = (int)((T_pad + AWQ_GROUP - 1) / AWQ_GROUP);
+    p.rows_tok = (int)K;
+    p.n_tiles = (int)(K / awq::kTcRows);
+    p.t_tiles = (int)((K + awq::kSearchTokensPerItem - 1) / awq::kSearchTokensPerItem);
+    p.n_items = p.n_tiles * p.t_tiles;
+    p.gout = G;
+    p.inv_t = (float)(1.0 / (double)T);
+    p.status = d->status;
+    e = awq::launch_tc_xtx(mapB, mapA, p, d->num_sms, st);
+    return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
+}
+
+size_t awq_search_gram_workspace_size(int64_t N, int64_t K, int n_alpha) {
+    if (N <= 0 || K <= 0 || n_alpha <= 0) return 0;
+    return search_ws(N, K, K, n_alpha).total;
+}
+
+awq_status awq_search_scale_gram(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                                 const uint16_t* G, const double* mean_abs, const double* alphas,
+                                 int n_alpha, int group, float* s_out, double* mse_out,
+                                 int32_t* best_idx, float* s_alpha_out, void* workspace,
+                                 size_t ws_bytes, awq_stream_t stream) {
+    const CallRange range("awq_search_scale_gram");
+    if (N <= 0 || K <= 0 || n_alpha < 1 || n_alpha > AWQ_MAX_ALPHAS)
+        return fail(AWQ_ERR_INVALID_ARG, "search_scale_gram: sizes must be positive, 1 <= n_alpha <= 64");
+    if (!W || !G || !mean_abs || !alphas || !s_out || !best_idx)
+        return fail(AWQ_ERR_INVALID_ARG, "search_scale_gram: null pointer");
+    if (group != AWQ_GROUP || K % AWQ_GROUP || N % 8 || ldw < K || ldw % 8)
+        return fail(AWQ_ERR_SHAPE, "search_scale_gram: need group 128, K % 128 == 0, N % 8 == 0, ldw >= K, ldw % 8 == 0");
+    if (N > (1LL << 30) || K > (1LL << 22))
+        return fail(AWQ_ERR_SHAPE, "search_scale_gram: size too large");
+    if (!aligned16(W) || !aligned16(G) || !aligned16(s_out) ||
+        (s_alpha_out && !aligned16(s_alpha_out)))
+        return fail(AWQ_ERR_ALIGN, "search_scale_gram: W, G, s_out must be 16-byte aligned");
+    const SearchWs lay = search_ws(N, K, K, n_alpha);
+    if (!workspace || ws_bytes < lay.total || !aligned16(workspace))
+        return fail(AWQ_ERR_WORKSPACE, "search_scale_gram: workspace missing or too small");
+    DevInfo* d = nullptr;
+    awq_status s = device_info(&d);
+    if (s) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* s_alpha = s_alpha_out ? s_alpha_out : reinterpret_cast<float*>(ws + lay.s_alpha);
+    float* inv_s = reinterpret_cast<float*>(ws + lay.inv_s);
+    double* partials = reinterpret_cast<double*>(ws + lay.partials);
+    double* mse = mse_out ? mse_out : reinterpret_cast<double*>(ws + lay.mse);
+    awq::AlphaList al;
+    for (int i = 0; i < n_alpha; ++i) al.a[i] = alphas[i];
+    cudaError_t e = awq::launch_candidate_scales(mean_abs, K, al, n_alpha, s_alpha, inv_s,
+                                                 reinterpret_cast<double*>(ws + lay.r),
+                                                 reinterpret_cast<double*>(ws + lay.mm), st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    CUtensorMap map;
+    s = make_act_map(&map, G, K, K, K);
+    if (s) return s;
+    awq::TcParams p = {};
+    p.N = (int)N;
+    p.K = (int)K;
+    p.G = (int)(K / AWQ_GROUP);
+    p.rows_tok = (int)K;
+    p.n_tiles = (int)((N + awq::kTcRows - 1) / awq::kTcRows);
+    p.t_tiles = (int)((K + awq::kSearchTokensPerItem - 1) / awq::kSearchTokensPerItem);
+    p.n_alpha = n_alpha;
+    p.n_items = p.n_tiles * p.t_tiles * n_alpha;
+    p.W = W;
+    p.ldw = ldw;
+    p.s_alpha = s_alpha;
+    p.inv_s_alpha = inv_s;
+    p.partials = partials;
+    p.status = d->status;
+    e = awq::launch_tc_gram_search(map, p, d->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    // G already carries the 1/T of the mean: divide the sums by N only
+    e = awq::launch_search_finalize(partials, n_alpha, (int64_t)p.n_tiles * p.t_tiles * 4, 1, N, K,
                                     s_alpha, mse, best_idx, s_out, st);
     return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
 }

@@ -102,6 +102,9 @@ struct TcParams {
     int n_alpha;
     double* partials;  // [n_alpha][n_tiles][t_tiles][4]
     unsigned* status;
+    // X^T X: fp16 out [N][rows_tok] (= [K][K]) scaled by inv_t
+    uint16_t* gout;
+    float inv_t;
 };
 constexpr int kTcRows = 128;          // weight rows per tile (UMMA M)
 constexpr int kTcTokens = 256;        // tokens per accumulator slot (UMMA N)
@@ -118,5 +121,16 @@ cudaError_t launch_splitk_reduce(const float* ws_partial, int k_splits, int64_t 
                                  uint16_t* Y, int64_t ldy, int num_sms, cudaStream_t st);
 cudaError_t launch_tc_search(const CUtensorMap& mapX, const TcParams& p, int num_sms,
                              cudaStream_t st);
+// G/T = X^T X / T into p.gout: both operands are tiles of X^T [K][T_pad]
+// (mapB: boxes of 64 x 256 rows, mapA: 64 x 128 rows).  p.N = p.rows_tok = K.
+cudaError_t launch_tc_xtx(const CUtensorMap& mapB, const CUtensorMap& mapA, const TcParams& p,
+                          int num_sms, cudaStream_t st);
+// The alpha search through G/T (mapG: G/T [K][K] fp16, boxes of 64 x 256
+// rows); partials as the direct search, already divided by T.
+cudaError_t launch_tc_gram_search(const CUtensorMap& mapG, const TcParams& p, int num_sms,
+                                  cudaStream_t st);
+// X^T [K][T_pad] (zero columns past T) from X [T][K] (leading dimension ldx).
+cudaError_t launch_transpose_x(const uint16_t* X, int64_t T, int64_t K, int64_t ldx,
+                               uint16_t* Xt, int64_t T_pad, cudaStream_t st);
 
 }  // namespace awq

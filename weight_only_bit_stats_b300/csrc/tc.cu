@@ -12,6 +12,15 @@
 //    E = Q(W diag(s)) diag(s)^-1 - W as fp16; the tensor cores form Xcal E^T
 //    and the epilogue reduces its squares -- the per-alpha output MSE is a
 //    fused epilogue and E never reaches global memory.
+//  * The same search through the Gram matrix: ||Xcal E^T||^2 = tr(E G E^T)
+//    with G = Xcal^T Xcal, so with G/T (fp16, [K, K]) in place of the
+//    calibration tokens the tensor cores form E (G/T), and the epilogue
+//    multiplies each accumulator column by the matching residual column --
+//    recomputed from W, s and the group parameters the producer exports --
+//    and adds.  The pages' grid search leaves the evaluation route open; this
+//    one costs 2 N K^2 per alpha instead of 2 T N K.
+//  * G/T itself: a plain fp16 GEMM of X^T with itself (both operands by TMA
+//    from a transposed copy of Xcal), scaled by 1/T and rounded to fp16.
 //
 // One persistent CTA per SM.  Warp roles:
 //   warp 0      TMA producer of activation tiles (one thread)
@@ -32,7 +41,7 @@
 namespace awq {
 namespace {
 
-enum { kModeGemm = 0, kModeSearch = 1 };
+enum { kModeGemm = 0, kModeSearch = 1, kModeXtX = 2, kModeGram = 3 };
 
 constexpr int kNA = 2;                            // A (weight) stages
 constexpr int kNB = 2;                            // B (activation) stages
@@ -46,21 +55,31 @@ constexpr int kWarpTma = 0, kWarpMma = 1, kWarpTmem = 2, kWarpEpi0 = 4, kWarpPro
 
 template <int MODE>
 struct Cfg {
-    static constexpr int kProdWarps = MODE == kModeGemm ? 4 : 16;
+    static constexpr int kProdWarps = MODE == kModeGemm ? 4 : (MODE == kModeXtX ? 0 : 16);
     static constexpr int kThreads = (kWarpProd0 + kProdWarps) * 32;
     static constexpr int kHalves = MODE == kModeGemm ? 1 : 2;   // accumulators per item
+};
+
+// Group parameters the Gram-search producer exports for the epilogue: for
+// the four groups of an item's 512 output columns, per tile row, the fp16
+// scale (as fp32), its reciprocal and the zero-point.  Two buffers (items
+// alternate).
+struct GramParams {
+    float scale[4][kTcRows], rcp[4][kTcRows], zf[4][kTcRows];
 };
 
 struct SmemCtl {
     uint64_t a_full[kNA], a_empty[kNA];
     uint64_t b_full[kNB], b_empty[kNB];
     uint64_t acc_full[2], acc_empty[2];
+    uint64_t par_full[2], par_empty[2];
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 /*align slack*/ + kNA * kAStage + kNB * kBStage + sizeof(SmemCtl);
+constexpr size_t kSmemBytes = 1024 /*align slack*/ + kNA * kAStage + kNB * kBStage +
+                              2 * sizeof(GramParams) + sizeof(SmemCtl);
 
 struct Item {
     int n_tile, t_tile, alpha;
@@ -89,6 +108,13 @@ __device__ __forceinline__ Item decode_item(int item, const TcParams& p) {
         it.alpha = 0;
         it.g0 = (int)((int64_t)it.split * p.G / p.k_splits);
         it.g1 = (int)((int64_t)(it.split + 1) * p.G / p.k_splits);
+    } else if (MODE == kModeXtX) {     // (row tile, column block) of X^T X
+        it.alpha = 0;
+        it.t_tile = item % p.t_tiles;
+        it.n_tile = item / p.t_tiles;
+        it.split = 0;
+        it.g0 = 0;
+        it.g1 = p.G;
     } else {                           // consecutive CTAs share the weight tile
         it.alpha = item % p.n_alpha;
         const int rest = item / p.n_alpha;
@@ -101,6 +127,11 @@ __device__ __forceinline__ Item decode_item(int item, const TcParams& p) {
     return it;
 }
 
+__device__ __forceinline__ uint32_t pack_h2_rn(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // Bounded wait that ignores the abort flag (used only to drain own copies).
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
     unsigned long long t0 = globaltimer_ns();
@@ -111,16 +142,29 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
 
 // ---- role: TMA producer of activation tiles ----
 template <int MODE>
-__device__ void role_tma(const CUtensorMap* mapX, const TcParams& p, uint8_t* Bs, SmemCtl* ctl) {
+__device__ void role_tma(const CUtensorMap* mapX, const CUtensorMap* mapA, const TcParams& p,
+                         uint8_t* As, uint8_t* Bs, SmemCtl* ctl) {
     constexpr int H = Cfg<MODE>::kHalves;
     volatile int* abort = &ctl->abort;
     // the activation tiles are re-read by every weight tile: keep them in L2
     const uint64_t pol = l2_policy_evict_last();
-    uint32_t b_iter = 0;
+    uint32_t a_iter = 0, b_iter = 0;
     for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
         const Item it = decode_item<MODE>(item, p);
         const int t0 = it.t_tile * kTcTokens * H;
         for (int g = it.g0; g < it.g1; ++g) {
+            if constexpr (MODE == kModeXtX) {
+                // the A operand is a tile of the same transposed matrix
+                const int st = a_iter % kNA;
+                if (!mbar_wait(&ctl->a_empty[st], ((a_iter / kNA) & 1u) ^ 1u, abort, p.status))
+                    goto drain;
+                mbar_arrive_expect_tx(&ctl->a_full[st], kAStage);
+                uint8_t* dst = As + st * kAStage;
+                tma_load_2d_hint(dst, mapA, &ctl->a_full[st], g * kGroup, it.n_tile * kTcRows, pol);
+                tma_load_2d_hint(dst + kASub, mapA, &ctl->a_full[st], g * kGroup + 64,
+                                 it.n_tile * kTcRows, pol);
+                ++a_iter;
+            }
             for (int h = 0; h < H; ++h) {
                 const int st = b_iter % kNB;
                 const uint32_t ph = (b_iter / kNB) & 1u;
@@ -140,6 +184,12 @@ drain:
     for (int d = 1; d <= kNB && (int)b_iter - d >= 0; ++d) {
         const uint32_t i = b_iter - d;
         mbar_drain(&ctl->b_full[i % kNB], (i / kNB) & 1u);
+    }
+    if constexpr (MODE == kModeXtX) {
+        for (int d = 1; d <= kNA && (int)a_iter - d >= 0; ++d) {
+            const uint32_t i = a_iter - d;
+            mbar_drain(&ctl->a_full[i % kNA], (i / kNA) & 1u);
+        }
     }
 }
 
@@ -193,24 +243,92 @@ out:
     mbar_drain(&ctl->mma_done, 0);
 }
 
+// Sum over 8 consecutive channels k0..k0+7 of one group of v[j] E[n, k0+j],
+// with the residual E of this thread's row recomputed from W, s, 1/s and the
+// group's exported parameters with the producer's arithmetic (so the fp16
+// values are the ones the tensor cores multiplied).  All 32 lanes call it
+// together (the exact-quotient vote).
+__device__ __forceinline__ float gram_dot8(const TcParams& p, const float* s_a, const float* is_a,
+                                           const uint16_t* wr, bool valid, int64_t k0, float scale,
+                                           float rcp, float neg_z, float top_z, const float* v) {
+    const uint4 raw = valid ? __ldg(reinterpret_cast<const uint4*>(wr + k0)) : make_uint4(0, 0, 0, 0);
+    const float4* sp = reinterpret_cast<const float4*>(s_a + k0);
+    const float4 s0 = __ldg(sp), s1 = __ldg(sp + 1);
+    const __half2* hh = reinterpret_cast<const __half2*>(&raw);
+    const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    float wp[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 f = __half22float2(hh[j]);
+        wp[2 * j] = __fmul_rn(f.x, sv[2 * j]);
+        wp[2 * j + 1] = __fmul_rn(f.y, sv[2 * j + 1]);
+    }
+    float r8[8];
+    rint_quot8(wp, scale, rcp, r8);
+    const float4* ip = reinterpret_cast<const float4*>(is_a + k0);
+    const float4 i0 = __ldg(ip), i1 = __ldg(ip + 1);
+    const float iv[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
+    float acc = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float qz = fminf(fmaxf(r8[j], neg_z), top_z);
+        const float ev = __fmul_rn(__fmaf_rn(qz, scale, -wp[j]), iv[j]);
+        acc = fmaf(v[j], __half2float(__float2half_rn(ev)), acc);
+    }
+    return acc;
+}
+
 // ---- role: epilogue ----
 template <int MODE>
-__device__ void role_epilogue(const TcParams& p, SmemCtl* ctl, uint32_t tmem, int q, int lane) {
+__device__ void role_epilogue(const TcParams& p, SmemCtl* ctl, const GramParams* gpar,
+                              uint32_t tmem, int q, int lane) {
     constexpr int H = Cfg<MODE>::kHalves;
     volatile int* abort = &ctl->abort;
-    uint32_t acc_iter = 0;
-    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+    uint32_t acc_iter = 0, item_iter = 0;
+    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++item_iter) {
         const Item it = decode_item<MODE>(item, p);
         const int64_t n = (int64_t)it.n_tile * kTcRows + q * 32 + lane;   // this thread's row
+        const int r = q * 32 + lane;                                       // row within the tile
         float sq = 0.0f;
+        double dsum = 0.0;
+        const GramParams* gp = gpar + (item_iter & 1);
         for (int h = 0; h < H; ++h) {
             const int slot = acc_iter & 1;
             if (!mbar_wait(&ctl->acc_full[slot], (acc_iter >> 1) & 1u, abort, p.status)) return;
             tc_fence_after();
+            if (MODE == kModeGram && h == 0) {
+                if (!mbar_wait(&ctl->par_full[item_iter & 1], (item_iter >> 1) & 1u, abort,
+                               p.status))
+                    return;
+            }
             const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * kTcTokens);
             const int64_t tok0 = ((int64_t)it.t_tile * H + h) * kTcTokens;
 #pragma unroll 1
             for (int c = 0; c < kTcTokens / 32; ++c) {
+                if constexpr (MODE == kModeGram) {
+                    // sum over these 32 columns of (E (G/T))[n, col] E[n, col],
+                    // 8 accumulator columns at a time
+                    const int64_t col = tok0 + c * 32;
+                    if (col < p.K) {                           // uniform over the warp
+                        const int gl = (int)(col / kGroup) - it.t_tile * 4;
+                        const float scale = gp->scale[gl][r], rcp = gp->rcp[gl][r];
+                        const float zf = gp->zf[gl][r];
+                        const bool valid = n < p.N;
+                        const uint16_t* wr = p.W + (valid ? n : 0) * p.ldw;
+                        const float* s_a = p.s_alpha + (int64_t)it.alpha * p.K;
+                        const float* is_a = p.inv_s_alpha + (int64_t)it.alpha * p.K;
+                        float acc = 0.0f;
+#pragma unroll 1
+                        for (int j = 0; j < 4; ++j) {
+                            float v8[8];
+                            tmem_ld8(taddr + c * 32 + 8 * j, v8);
+                            acc += gram_dot8(p, s_a, is_a, wr, valid, col + 8 * j, scale, rcp, -zf,
+                                             15.0f - zf, v8);
+                        }
+                        if (valid) dsum += (double)acc;
+                    }
+                    continue;
+                }
                 float v[32];
                 tmem_ld32(taddr + c * 32, v);
                 if (MODE == kModeGemm) {
@@ -233,6 +351,19 @@ __device__ void role_epilogue(const TcParams& p, SmemCtl* ctl, uint32_t tmem, in
                             }
                         }
                     }
+                } else if (MODE == kModeXtX) {
+                    // G/T: 32 consecutive columns of row n, as fp16
+                    const int64_t col = tok0 + c * 32;
+                    if (n < p.N && col < p.rows_tok) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            w[j] = pack_h2_rn(v[2 * j] * p.inv_t, v[2 * j + 1] * p.inv_t);
+                        uint4* dst = reinterpret_cast<uint4*>(p.gout + n * p.rows_tok + col);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                    }
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) sq = fmaf(v[j], v[j], sq);
@@ -242,6 +373,15 @@ __device__ void role_epilogue(const TcParams& p, SmemCtl* ctl, uint32_t tmem, in
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->acc_empty[slot]);
             ++acc_iter;
+        }
+        if (MODE == kModeGram) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->par_empty[item_iter & 1]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+            if (lane == 0)
+                p.partials[(((int64_t)it.alpha * p.n_tiles + it.n_tile) * p.t_tiles + it.t_tile) * 4 +
+                           q] = dsum;
         }
         if (MODE == kModeSearch) {
             // one fp64 partial per epilogue warp; the final reduction adds
@@ -404,8 +544,9 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-template <int PW>
-__device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, int pw, int lane) {
+template <int PW, bool GRAM>
+__device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, GramParams* gpar,
+                                 int pw, int lane) {
     static_assert(PW * 8 == kTcRows, "16 producer warps x 8 rows");
     volatile int* abort = &ctl->abort;
     const int rr = lane >> 2, c = lane & 3;
@@ -414,10 +555,17 @@ __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, i
     // + 32 (q % 2)); within a sub-tile the two chunks sit 64 bytes apart after the
     // swizzle (chunk index XOR row % 8 flips only its low three bits)
     const uint32_t soff0 = sw128_offset(r, 8 * c);
-    uint32_t a_iter = 0;
+    uint32_t a_iter = 0, item_iter = 0;
     bool bad = false;
-    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++item_iter) {
         const Item it = decode_item<kModeSearch>(item, p);
+        // Gram route: the groups of this item's 512 output columns, whose
+        // parameters the epilogue needs (exported into buffer item_iter % 2)
+        const int g_par = it.t_tile * 4;
+        GramParams* gp = gpar + (item_iter & 1);
+        if (GRAM && !mbar_wait(&ctl->par_empty[item_iter & 1], ((item_iter >> 1) & 1u) ^ 1u, abort,
+                               p.status))
+            return;
         const float* s_a = p.s_alpha + (int64_t)it.alpha * p.K;
         const float* is_a = p.inv_s_alpha + (int64_t)it.alpha * p.K;
         const int64_t n = (int64_t)it.n_tile * kTcRows + r;
@@ -457,6 +605,11 @@ __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, i
             }
             const GroupQuant gq = group_quant_from_range(lo, hi);
             bad |= !gq.finite;
+            if (GRAM && c == 0 && g >= g_par && g < g_par + 4) {
+                gp->scale[g - g_par][r] = gq.scale;
+                gp->rcp[g - g_par][r] = gq.rcp;
+                gp->zf[g - g_par][r] = gq.zf;
+            }
             const float neg_z = -gq.zf, top_z = 15.0f - gq.zf;
             const int st = a_iter % kNA;
             if (!mbar_wait(&ctl->a_empty[st], ((a_iter / kNA) & 1u) ^ 1u, abort, p.status)) return;
@@ -486,24 +639,31 @@ __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, i
             if (lane == 0) mbar_arrive(&ctl->a_full[st]);
             ++a_iter;
         }
+        if (GRAM) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->par_full[item_iter & 1]);
+        }
     }
     if (bad) set_status(p.status, kStatusNonFinite);
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
-    tc_kernel(const __grid_constant__ CUtensorMap mapX, const TcParams p) {
+    tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapA,
+              const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* As = smem;
     uint8_t* Bs = smem + kNA * kAStage;
-    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(Bs + kNB * kBStage);
+    GramParams* gpar = reinterpret_cast<GramParams*>(Bs + kNB * kBStage);
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(gpar + 2);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNA; ++i) {
-            mbar_init(&ctl->a_full[i], Cfg<MODE>::kProdWarps);
+            // the A stages are filled by the producer warps, or by TMA (X^T X)
+            mbar_init(&ctl->a_full[i], Cfg<MODE>::kProdWarps > 0 ? Cfg<MODE>::kProdWarps : 1);
             mbar_init(&ctl->a_empty[i], 1);
         }
         for (int i = 0; i < kNB; ++i) {
@@ -513,6 +673,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctl->acc_full[i], 1);
             mbar_init(&ctl->acc_empty[i], 4);
+            mbar_init(&ctl->par_full[i], Cfg<MODE>::kProdWarps > 0 ? Cfg<MODE>::kProdWarps : 1);
+            mbar_init(&ctl->par_empty[i], 4);
         }
         mbar_init(&ctl->mma_done, 1);
         ctl->abort = 0;
@@ -522,23 +684,30 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
         tmem_alloc(&ctl->tmem_base, kTmemCols);
         tmem_relinquish();
     }
-    if (warp == kWarpTma && lane == 0) tma_prefetch_desc(&mapX);
+    if (warp == kWarpTma && lane == 0) {
+        tma_prefetch_desc(&mapX);
+        if (MODE == kModeXtX) tma_prefetch_desc(&mapA);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
 
     if (warp == kWarpTma) {
-        if (lane == 0) role_tma<MODE>(&mapX, p, Bs, ctl);
+        if (lane == 0) role_tma<MODE>(&mapX, &mapA, p, As, Bs, ctl);
     } else if (warp == kWarpMma) {
         if (lane == 0) role_mma<MODE>(p, As, Bs, ctl, tmem);
     } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
-        role_epilogue<MODE>(p, ctl, tmem, warp - kWarpEpi0, lane);
+        role_epilogue<MODE>(p, ctl, gpar, tmem, warp - kWarpEpi0, lane);
     } else if (warp >= kWarpProd0) {
         if constexpr (MODE == kModeGemm)
             role_prod_gemm(p, As, ctl, (warp - kWarpProd0) * 32 + lane, lane);
-        else
-            role_prod_search<Cfg<MODE>::kProdWarps>(p, As, ctl, warp - kWarpProd0, lane);
+        else if constexpr (MODE == kModeSearch)
+            role_prod_search<Cfg<MODE>::kProdWarps, false>(p, As, ctl, gpar, warp - kWarpProd0,
+                                                           lane);
+        else if constexpr (MODE == kModeGram)
+            role_prod_search<Cfg<MODE>::kProdWarps, true>(p, As, ctl, gpar, warp - kWarpProd0,
+                                                          lane);
     }
 
     tc_fence_before();
@@ -550,12 +719,13 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
 }
 
 template <int MODE>
-cudaError_t launch_tc(const CUtensorMap& mapX, const TcParams& p, int num_sms, cudaStream_t st) {
+cudaError_t launch_tc(const CUtensorMap& mapX, const CUtensorMap& mapA, const TcParams& p,
+                      int num_sms, cudaStream_t st) {
     if (p.n_items <= 0) return cudaSuccess;
     cudaError_t e = smem_attr_once<tc_kernel<MODE>>((int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = p.n_items < num_sms ? p.n_items : num_sms;
-    tc_kernel<MODE><<<grid, Cfg<MODE>::kThreads, kSmemBytes, st>>>(mapX, p);
+    tc_kernel<MODE><<<grid, Cfg<MODE>::kThreads, kSmemBytes, st>>>(mapX, mapA, p);
     return cudaGetLastError();
 }
 
@@ -585,11 +755,19 @@ cudaError_t launch_splitk_reduce(const float* ws_partial, int k_splits, int64_t 
 
 cudaError_t launch_tc_gemm(const CUtensorMap& mapX, const TcParams& p, int num_sms,
                            cudaStream_t st) {
-    return launch_tc<kModeGemm>(mapX, p, num_sms, st);
+    return launch_tc<kModeGemm>(mapX, mapX, p, num_sms, st);
 }
 cudaError_t launch_tc_search(const CUtensorMap& mapX, const TcParams& p, int num_sms,
                              cudaStream_t st) {
-    return launch_tc<kModeSearch>(mapX, p, num_sms, st);
+    return launch_tc<kModeSearch>(mapX, mapX, p, num_sms, st);
+}
+cudaError_t launch_tc_xtx(const CUtensorMap& mapB, const CUtensorMap& mapA, const TcParams& p,
+                          int num_sms, cudaStream_t st) {
+    return launch_tc<kModeXtX>(mapB, mapA, p, num_sms, st);
+}
+cudaError_t launch_tc_gram_search(const CUtensorMap& mapG, const TcParams& p, int num_sms,
+                                  cudaStream_t st) {
+    return launch_tc<kModeGram>(mapG, mapG, p, num_sms, st);
 }
 
 }  // namespace awq
