@@ -63,6 +63,10 @@ def search_flop(N, K, T=T_CAL, n_alpha=N_ALPHA):
     return 2.0 * T * N * K * n_alpha
 
 
+def search_flop_t(N, K, T=128 * 512, n_alpha=N_ALPHA):
+    return 2.0 * T * N * K * n_alpha
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -306,6 +310,10 @@ def run_ours(args, rank, world):
     # (all repetitions are queued before any is read, so the host never
     # leaves the GPU idle inside a timed launch)
     def alone(launch):
+        # the host queues every repetition while the GPU sleeps, so no launch
+        # waits for the host inside its events
+        torch.cuda.synchronize()
+        torch.cuda._sleep(100_000_000)
         evs_alone = []
         for _ in range(20):
             flush_w.fill_(1.0)
@@ -327,6 +335,8 @@ def run_ours(args, rank, world):
     # the same four-launch decode segment on the plain packed layout
     # (w4a16_gemm), for comparison with the repacked tiles
     seg_plain = []
+    torch.cuda.synchronize()
+    torch.cuda._sleep(100_000_000)
     for _ in range(20):
         flush_w.fill_(1.0)
         torch.sum(flush_r, dim=0, out=flush_out)
@@ -347,6 +357,8 @@ def run_ours(args, rank, world):
     read_ms = []
     for p in projs:
         buf = torch.ones(gemv_bytes(p["N"], p["K"]) // 4, dtype=torch.float32, device=dev)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(100_000_000)
         evs_read = []
         for _ in range(20):
             flush_w.fill_(1.0)
@@ -445,6 +457,189 @@ def run_ours(args, rank, world):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args, budget_s=args.cpu_budget, projs=projs)
     return out
+
+
+# ------------------------------------------------- full LLaMA-7B pass --
+
+FULL_T = 128 * 512                 # calibration tokens per layer input
+FULL_M = (1, 16, 64, 256)
+FULL_WORKLOAD = ("full LLaMA-7B-shaped quantisation pass: per decoder layer, statistics of its "
+                 "four inputs over 128 x 512 = 65536 calibration tokens, G/T = X^T X / T per "
+                 "input, the 20-alpha search of each of the 7 linears (q, k, v, o 4096x4096; "
+                 "gate, up 11008x4096; down 4096x11008) through G/T, INT4 g128 pack and decode "
+                 "repack, then w4a16 matmuls at M in {1, 16, 64, 256}; W ~ N(0,0.02^2), X ~ "
+                 "N(0,1) with 1% channels x20")
+
+
+def gram_flop(N, K, n_alpha=N_ALPHA):
+    return 2.0 * N * K * K * n_alpha
+
+
+def run_full_pass(args, rank, world):
+    """BASELINE's fifth workload on a sample of decoder layers: one step is
+    one layer's whole pass.  The layers' inputs (3 GB of calibration tokens
+    per layer) are generated on the host and uploaded before the timed region;
+    they exceed L2 many times over, so no flush is needed."""
+    import torch
+    import weight_only_bit_stats_b300 as wb
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    n_layers = max(1, args.steps)
+    layer_ids = [(rank * n_layers + i) % 32 for i in range(n_layers)]
+    t_gen = time.perf_counter()
+    layers = []
+    for li in layer_ids:
+        L = {"id": li, "x": [], "lin": []}
+        for idx, (name, K) in enumerate(sg.LLAMA7B_LAYER_INPUTS):
+            L["x"].append(torch.from_numpy(sg.layer_activations(li, idx, FULL_T, K)).to(dev))
+        for j, (name, N, K) in enumerate(sg.LLAMA7B_LAYER_LINEARS):
+            W, _, Xm, _ = sg.layer_inputs(li, j, N, K, 0, M=max(FULL_M))
+            L["lin"].append(dict(name=name, N=N, K=K, W=torch.from_numpy(W).to(dev),
+                                 xm=torch.from_numpy(Xm).to(dev)))
+        layers.append(L)
+    t_gen = time.perf_counter() - t_gen
+    # buffers shared by every layer
+    ws_gram = {K: torch.empty(wb.lib().awq_gram_workspace_size(FULL_T, K), dtype=torch.uint8,
+                              device=dev) for _, K in sg.LLAMA7B_LAYER_INPUTS}
+    G = {idx: torch.empty((K, K), dtype=torch.float16, device=dev)
+         for idx, (_, K) in enumerate(sg.LLAMA7B_LAYER_INPUTS)}
+    abs_sum = {idx: torch.empty(K, dtype=torch.int64, device=dev)
+               for idx, (_, K) in enumerate(sg.LLAMA7B_LAYER_INPUTS)}
+    mean = {idx: torch.empty(K, dtype=torch.float64, device=dev)
+            for idx, (_, K) in enumerate(sg.LLAMA7B_LAYER_INPUTS)}
+    out = []
+    for j, (name, N, K) in enumerate(sg.LLAMA7B_LAYER_LINEARS):
+        out.append(dict(
+            s=torch.empty(K, dtype=torch.float32, device=dev),
+            mse=torch.empty(N_ALPHA, dtype=torch.float64, device=dev),
+            best=torch.empty(1, dtype=torch.int32, device=dev),
+            ws=torch.empty(max(16, wb.lib().awq_search_gram_workspace_size(N, K, N_ALPHA)),
+                           dtype=torch.uint8, device=dev),
+            qw=torch.empty((N, K // 8), dtype=torch.int32, device=dev),
+            sc=torch.empty((N, K // 128), dtype=torch.float16, device=dev),
+            ze=torch.empty((N, K // 128), dtype=torch.float16, device=dev),
+            tiles=torch.empty(wb.lib().awq_repack_int4_bytes(N, K), dtype=torch.uint8, device=dev),
+            y=torch.empty((max(FULL_M), N), dtype=torch.float16, device=dev),
+            gws=torch.empty(max(16, max(wb.lib().w4a16_gemm_workspace_size(M, N, K)
+                                        for M in FULL_M)), dtype=torch.uint8, device=dev)))
+    stream = torch.cuda.current_stream()
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    stages = ("stats", "gram", "search", "pack", "matmul_m1", "matmul_m16", "matmul_m64",
+              "matmul_m256")
+
+    def step(L, ev=None):
+        rec = (lambda k: ev[k].record(stream)) if ev else (lambda k: None)
+        rec(0)
+        for idx, X in enumerate(L["x"]):
+            wb.act_stats(X, out=abs_sum[idx])
+            wb.act_mean(abs_sum[idx], FULL_T, out=mean[idx])
+        rec(1)
+        for idx, X in enumerate(L["x"]):
+            wb.gram(X, out=G[idx], workspace=ws_gram[X.shape[1]])
+        rec(2)
+        for j, lin in enumerate(L["lin"]):
+            idx = sg.LLAMA7B_LINEAR_INPUT[j]
+            o = out[j]
+            wb.search_scale_gram(lin["W"], G[idx], mean[idx], workspace=o["ws"],
+                                 out=(o["s"], o["mse"], o["best"]))
+        rec(3)
+        for j, lin in enumerate(L["lin"]):
+            o = out[j]
+            wb.pack_int4(lin["W"], o["s"], out=(o["qw"], o["sc"], o["ze"]))
+            wb.repack_int4(o["qw"], o["sc"], o["ze"], out=o["tiles"])
+        rec(4)
+        for k, M in enumerate(FULL_M):
+            for j, lin in enumerate(L["lin"]):
+                o = out[j]
+                if M <= 16:
+                    wb.w4a16_gemm_repacked(lin["xm"][:M], o["tiles"], lin["N"], out=o["y"][:M])
+                else:
+                    wb.w4a16_gemm(lin["xm"][:M], o["qw"], o["sc"], o["ze"], out=o["y"][:M])
+            rec(5 + k)
+
+    for _ in range(max(3, args.warmup)):
+        step(layers[0])
+    wb.sync_status()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.3)
+    evs = [[E() for _ in range(len(stages) + 1)] for _ in layers]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = E(), E()
+    if sampler: sampler.mark_start()
+    t0.record(stream)
+    for L, ev in zip(layers, evs):
+        step(L, ev)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if sampler: sampler.mark_end()
+    if world > 1:
+        dist.barrier()
+    wb.sync_status()
+    total_ms = max_over_ranks([t0.elapsed_time(t1)], dev)[0]
+    st = {k: 0.0 for k in stages}
+    for ev in evs:
+        for k, name in enumerate(stages):
+            st[name] += ev[k].elapsed_time(ev[k + 1])
+    clocks = sampler.stop() if sampler else None
+    nl = len(layers)
+    lin = sg.LLAMA7B_LAYER_LINEARS
+    inputs = sg.LLAMA7B_LAYER_INPUTS
+    gram_form_flop = sum(2.0 * FULL_T * K * K for _, K in inputs)
+    search_flop = sum(gram_flop(N, K) for _, N, K in lin)
+    direct_flop = sum(search_flop_t(N, K) for _, N, K in lin)
+    bytes_m = {M: sum(gemv_bytes(N, K, M) for _, N, K in lin) for M in FULL_M}
+    flop_m = {M: sum(2.0 * M * N * K for _, N, K in lin) for M in FULL_M}
+    mm = {}
+    for k, M in enumerate(FULL_M):
+        ms = st[stages[4 + k]] / nl
+        mm[f"M={M}"] = {"ms": round(ms, 4), "gbs": round(bytes_m[M] / (ms * 1e-3) / 1e9, 1),
+                        "tflops": round(flop_m[M] / (ms * 1e-3) / 1e12, 2)}
+    value = job_value(bytes_m[1], nl, max_over_ranks([st["matmul_m1"]], dev)[0], world)
+    peaks, peak_src = load_peaks()
+    search_tf = search_flop * nl / (st["search"] * 1e-3) / 1e12
+    peak_key, peak_kind = (("bf16_tflops", "burst") if total_ms < 1000.0
+                           else ("bf16_tflops_sustained", "sustained"))
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": nl, "warmup": max(3, args.warmup), "ms_per_step": round(total_ms / nl, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": FULL_WORKLOAD + f"; sample of {nl} of the 32 decoder layers "
+                                               f"(layers {layer_ids})",
+                   "calibration_tokens": FULL_T, "alphas": N_ALPHA, "M": list(FULL_M),
+                   "search_route": "Gram matrix (awq_gram + awq_search_scale_gram)",
+                   "l2": "inputs exceed L2 (3 GB of calibration tokens per layer)",
+                   "value_basis": "M = 1 matmul algorithmic bytes of the 7 linears / CUDA-event "
+                                  "time of the M = 1 segment, per layer",
+                   "parallelism": f"replicas x{world} (own layers per GPU, no collective)"},
+        "seconds_per_layer": round(total_ms / nl / 1e3, 4),
+        "projected_32_layers_s": round(32 * total_ms / nl / 1e3, 3),
+        "stages_ms_per_layer": {k: round(v / nl, 4) for k, v in st.items()},
+        "roofline": {"kernel": "tc_kernel<3> (Gram-route search: fake-quant producer + tcgen05 "
+                               "E (G/T) + residual-column epilogue)",
+                     "bound": "tensor", "achieved": round(search_tf, 2),
+                     "peak": peaks[peak_key], "unit": "TFLOP/s",
+                     "frac": round(search_tf / peaks[peak_key], 4),
+                     "peak_source": f"{peak_src} bf16 dense {peak_kind} (fp16 nominal = bf16)",
+                     "traffic": None,
+                     "timing": "CUDA events around the 7 awq_search_scale_gram calls of a layer"},
+        "search": {"gram_route_flop_per_layer": search_flop,
+                   "gram_formation_flop_per_layer": gram_form_flop,
+                   "direct_route_flop_per_layer": direct_flop,
+                   "gram_formation_tflops": round(gram_form_flop * nl / (st["gram"] * 1e-3) / 1e12,
+                                                  1),
+                   "direct_equivalent_tflops": round(direct_flop * nl / ((st["search"] + st["gram"])
+                                                                        * 1e-3) / 1e12, 1)},
+        "matmul_per_layer": mm,
+        "host_generation_s": round(t_gen, 1),
+        "gpu_launches": nl * (4 * 2 + 4 * 2 + 7 * 4 + 7 * 2 + 7 * len(FULL_M)),
+        "clocks": clocks,
+    }
+    return res
 
 
 PREFILL_M = (256, 1024, 4096)
@@ -673,7 +868,9 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 50; with --workload llama7b_full: decoder "
+                         "layers, default 2)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
@@ -681,7 +878,13 @@ def main():
                     help="do not report the separate M >= 256 GEMM measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--workload", choices=["llama7b_decode", "llama7b_full"],
+                    default="llama7b_decode",
+                    help="llama7b_full: the full LLaMA-7B quantisation pass, one step per "
+                         "decoder layer (steps = layers sampled)")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 2 if args.workload == "llama7b_full" else 50
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
 
@@ -695,7 +898,8 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
-    out = run_ours(args, rank, world)
+    out = run_full_pass(args, rank, world) if args.workload == "llama7b_full" else \
+        run_ours(args, rank, world)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -78,8 +78,14 @@ struct SmemCtl {
     int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 /*align slack*/ + kNA * kAStage + kNB * kBStage +
-                              2 * sizeof(GramParams) + sizeof(SmemCtl);
+// Shared memory per mode: the Gram route's parameter buffers only where they
+// are used, so the other modes keep more of the SM's L1 (the GEMM producer's
+// packed-word loads and the search producer's scale loads go through it).
+template <int MODE>
+constexpr size_t smem_bytes() {
+    return 1024 /*align slack*/ + (size_t)kNA * kAStage + (size_t)kNB * kBStage +
+           (MODE == kModeGram ? 2 * sizeof(GramParams) : 0) + sizeof(SmemCtl);
+}
 
 struct Item {
     int n_tile, t_tile, alpha;
@@ -657,7 +663,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     uint8_t* As = smem;
     uint8_t* Bs = smem + kNA * kAStage;
     GramParams* gpar = reinterpret_cast<GramParams*>(Bs + kNB * kBStage);
-    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(gpar + 2);
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(Bs + kNB * kBStage +
+                                              (MODE == kModeGram ? 2 * sizeof(GramParams) : 0));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -722,10 +729,11 @@ template <int MODE>
 cudaError_t launch_tc(const CUtensorMap& mapX, const CUtensorMap& mapA, const TcParams& p,
                       int num_sms, cudaStream_t st) {
     if (p.n_items <= 0) return cudaSuccess;
-    cudaError_t e = smem_attr_once<tc_kernel<MODE>>((int)kSmemBytes);
+    constexpr size_t kSmem = smem_bytes<MODE>();
+    cudaError_t e = smem_attr_once<tc_kernel<MODE>>((int)kSmem);
     if (e != cudaSuccess) return e;
     const int grid = p.n_items < num_sms ? p.n_items : num_sms;
-    tc_kernel<MODE><<<grid, Cfg<MODE>::kThreads, kSmemBytes, st>>>(mapX, mapA, p);
+    tc_kernel<MODE><<<grid, Cfg<MODE>::kThreads, kSmem, st>>>(mapX, mapA, p);
     return cudaGetLastError();
 }
 
