@@ -131,6 +131,17 @@ awq_status awq_search_scale(const uint16_t* W, int64_t N, int64_t K, int64_t ldw
                             awq_stream_t stream);
 size_t awq_search_workspace_size(int64_t N, int64_t K, int64_t T, int n_alpha);
 
+/* The same search at 3 bits (the pages evaluate 3 and 4 bits, fourth
+ * paragraph): the fake quantiser is awq_pack_int3's (levels 0..7, scale =
+ * fp16_rn(max(fp32(range / 7), 2^-14)), zero-point clamped to 0..7).
+ * Arguments, results and workspace as awq_search_scale. */
+awq_status awq_search_scale_int3(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                                 const uint16_t* Xcal, int64_t T, int64_t ldx,
+                                 const double* mean_abs, const double* alphas, int n_alpha,
+                                 int group, float* s_out, double* mse_out, int32_t* best_idx,
+                                 float* s_alpha_out, void* workspace, size_t ws_bytes,
+                                 awq_stream_t stream);
+
 /* ---- alpha search through the Gram matrix ---------------------------------
  * The pages' "quick grid search on a small calibration set" (third paragraph)
  * fixes the objective, not how it is evaluated.  ||Xcal E^T||_F^2 =
@@ -164,6 +175,12 @@ awq_status awq_search_scale_gram(const uint16_t* W, int64_t N, int64_t K, int64_
                                  int n_alpha, int group, float* s_out, double* mse_out,
                                  int32_t* best_idx, float* s_alpha_out, void* workspace,
                                  size_t ws_bytes, awq_stream_t stream);
+/* The Gram-route search at 3 bits (levels 0..7 as awq_search_scale_int3). */
+awq_status awq_search_scale_gram_int3(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                                      const uint16_t* G, const double* mean_abs,
+                                      const double* alphas, int n_alpha, int group, float* s_out,
+                                      double* mse_out, int32_t* best_idx, float* s_alpha_out,
+                                      void* workspace, size_t ws_bytes, awq_stream_t stream);
 
 /* ---- alpha search without any device allocation ---------------------------
  * No counterpart on the AWQ pages: an allocation-free variant of
@@ -223,13 +240,17 @@ awq_status awq_pack_int3(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
                          const float* s, int group, uint32_t* planes, uint16_t* scales,
                          uint16_t* zeros, awq_stream_t stream);
 
-/* ---- step: 3-bit decode matmul -----------------------------------------------
+/* ---- step: 3-bit matmul ---------------------------------------------------------
  * Y = X deq(Wq)^T over the 3-bit format of awq_pack_int3, deq = (q - z) *
- * scale, fp32 accumulation, fp16 out, for 1 <= M <= 16 tokens (decoding,
+ * scale, fp32 accumulation, fp16 out.  For 1 <= M <= 16 tokens (decoding,
  * the memory-bound case; AWQ page sixth paragraph: fewer bytes per weight,
- * faster tokens at small batch).  Arguments as w4a16_gemm, with planes
- * [N, 3K/32] uint32 in place of qweight.  M > 16 returns AWQ_ERR_SHAPE.
- * X 16-byte aligned, ldx a multiple of 8; planes 4-byte aligned. */
+ * faster tokens at small batch) the planes are streamed and the products
+ * summed per group; for M > 16 (AWQ page ninth paragraph: larger batches
+ * are compute-bound) the tcgen05 tensor-core GEMM runs with a producer that
+ * rebuilds each (q - z) exactly in fp16 and rounds (q - z) * scale once to
+ * fp16.  Arguments as w4a16_gemm, with planes [N, 3K/32] uint32 in place of
+ * qweight and no workspace.  X 16-byte aligned, ldx a multiple of 8; planes
+ * 4-byte aligned (16-byte for M > 16). */
 awq_status w3a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
                       const uint32_t* planes, const uint16_t* scales, const uint16_t* zeros,
                       int64_t N, int group, uint16_t* Y, int64_t ldy, awq_stream_t stream);

@@ -99,8 +99,8 @@ def test_host_argument_checks(capi):
     assert capi.awq_pack_int3(base, 8, 96, 96, None, 128, base, base, base, None) == 2
     assert capi.awq_pack_int3(base + 2, 8, 128, 128, None, 128, base, base, base, None) == 3
     assert capi.awq_pack_int3(base, 8, 128, 128, None, 128, base + 2, base, base, None) == 3
-    # 3-bit matmul: decode sizes only (M <= 16), N % 8, misaligned X
-    assert capi.w3a16_gemm(base, 17, 128, 128, base, base, base, 8, 128, base, 8, None) == 2
+    # 3-bit matmul: planes 16-byte aligned for M > 16 (tensor-core path), N % 8, misaligned X
+    assert capi.w3a16_gemm(base, 17, 128, 128, base + 4, base, base, 8, 128, base, 8, None) == 3
     assert capi.w3a16_gemm(base, 1, 128, 128, base, base, base, 12, 128, base, 12, None) == 2
     assert capi.w3a16_gemm(base + 2, 1, 128, 128, base, base, base, 8, 128, base, 8, None) == 3
     assert capi.w3a16_gemm(None, 1, 128, 128, base, base, base, 8, 128, base, 8, None) == 1

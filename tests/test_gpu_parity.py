@@ -235,15 +235,6 @@ def test_w3a16_decode_long_k(wb, orc, M, N, K):
     wb.sync_status()
 
 
-def test_w3a16_refuses_prefill_sizes(wb):
-    x = torch.zeros((17, 128), dtype=torch.float16, device="cuda")
-    pl = torch.zeros((8, 12), dtype=torch.int32, device="cuda")
-    sc = torch.zeros((8, 1), dtype=torch.float16, device="cuda")
-    with pytest.raises(wb.AwqError) as e:
-        wb.w3a16_gemm(x, pl, sc, sc)
-    assert e.value.code == 2
-
-
 # ---------------------------------------------------------- a2-a4 search --
 
 def _search_check(wb, orc, W, X, alphas=None):

@@ -77,6 +77,10 @@ SIGNATURES = (
     ("awq_search_gram_workspace_size", _sz, [_i64, _i64, _int]),
     ("awq_search_scale_gram", _int, [_p, _i64, _i64, _i64, _p, _p, _p, _int, _int, _p, _p, _p, _p,
                                      _p, _sz, _p]),
+    ("awq_search_scale_gram_int3", _int, [_p, _i64, _i64, _i64, _p, _p, _p, _int, _int, _p, _p, _p,
+                                          _p, _p, _sz, _p]),
+    ("awq_search_scale_int3", _int, [_p, _i64, _i64, _i64, _p, _i64, _i64, _p, _p, _int, _int, _p,
+                                     _p, _p, _p, _p, _sz, _p]),
     ("awq_repack_int4", _int, [_p, _p, _p, _i64, _i64, _int, _p, _sz, _p]),
     ("w4a16_gemm_repacked", _int, [_p, _i64, _i64, _i64, _p, _p, _i64, _int, _p, _i64, _p]),
     ("awq_set_weight_prefetch", _int, [_int]),
@@ -199,9 +203,11 @@ def gram(Xcal: torch.Tensor, out: torch.Tensor | None = None, workspace: torch.T
 
 def search_scale_gram(W: torch.Tensor, G: torch.Tensor, mean_abs: torch.Tensor,
                       alphas=ALPHA_GRID, workspace: torch.Tensor | None = None,
-                      return_candidates: bool = False, out=None, stream=None):
+                      return_candidates: bool = False, out=None, stream=None, bits: int = 4):
     """The alpha search through G/T from ``gram``: returns (s, mse, best)
     like ``search_scale`` (and the candidate scales when asked)."""
+    if bits not in (3, 4):
+        raise ValueError("bits must be 3 or 4")
     _dev(W, torch.float16, "W")
     _dev(G, torch.float16, "G")
     _dev(mean_abs, torch.float64, "mean_abs")
@@ -217,20 +223,24 @@ def search_scale_gram(W: torch.Tensor, G: torch.Tensor, mean_abs: torch.Tensor,
     n = lib().awq_search_gram_workspace_size(N, K, na)
     if workspace is None:
         workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=W.device)
-    _check(lib().awq_search_scale_gram(W.data_ptr(), N, K, _ld(W), G.data_ptr(), mean_abs.data_ptr(),
-                                       arr, na, GROUP, s.data_ptr(), mse.data_ptr(), best.data_ptr(),
-                                       cand.data_ptr() if cand is not None else None,
-                                       workspace.data_ptr(), workspace.numel(), _stream(stream)),
-           "awq_search_scale_gram")
+    fn = lib().awq_search_scale_gram if bits == 4 else lib().awq_search_scale_gram_int3
+    _check(fn(W.data_ptr(), N, K, _ld(W), G.data_ptr(), mean_abs.data_ptr(),
+              arr, na, GROUP, s.data_ptr(), mse.data_ptr(), best.data_ptr(),
+              cand.data_ptr() if cand is not None else None,
+              workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "awq_search_scale_gram" if bits == 4 else "awq_search_scale_gram_int3")
     return (s, mse, best, cand) if return_candidates else (s, mse, best)
 
 
 def search_scale(W: torch.Tensor, Xcal: torch.Tensor, mean_abs: torch.Tensor, alphas=ALPHA_GRID,
                  workspace: torch.Tensor | None = None, return_candidates: bool = False,
-                 out=None, stream=None):
-    """alpha grid search.  Returns ``(s fp32 [K], mse fp64 [n_alpha],
-    best int32 [1])`` (+ all candidate scales [n_alpha, K] when
-    ``return_candidates``), all on the device."""
+                 out=None, stream=None, bits: int = 4):
+    """alpha grid search (``bits`` 4, or 3 for the levels of ``pack_int3``).
+    Returns ``(s fp32 [K], mse fp64 [n_alpha], best int32 [1])`` (+ all
+    candidate scales [n_alpha, K] when ``return_candidates``), all on the
+    device."""
+    if bits not in (3, 4):
+        raise ValueError("bits must be 3 or 4")
     _dev(W, torch.float16, "W")
     _dev(Xcal, torch.float16, "Xcal")
     _dev(mean_abs, torch.float64, "mean_abs")
@@ -247,11 +257,12 @@ def search_scale(W: torch.Tensor, Xcal: torch.Tensor, mean_abs: torch.Tensor, al
     cands = torch.empty((n, K), dtype=torch.float32, device=dev) if return_candidates else None
     if workspace is None:
         workspace = search_workspace(N, K, T, n, dev)
-    _check(lib().awq_search_scale(W.data_ptr(), N, K, _ld(W), Xcal.data_ptr(), T, _ld(Xcal),
-                                  mean_abs.data_ptr(), arr, n, GROUP, s.data_ptr(), mse.data_ptr(),
-                                  best.data_ptr(), cands.data_ptr() if cands is not None else None,
-                                  workspace.data_ptr(), workspace.numel(), _stream(stream)),
-           "awq_search_scale")
+    fn = lib().awq_search_scale if bits == 4 else lib().awq_search_scale_int3
+    _check(fn(W.data_ptr(), N, K, _ld(W), Xcal.data_ptr(), T, _ld(Xcal),
+              mean_abs.data_ptr(), arr, n, GROUP, s.data_ptr(), mse.data_ptr(),
+              best.data_ptr(), cands.data_ptr() if cands is not None else None,
+              workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "awq_search_scale" if bits == 4 else "awq_search_scale_int3")
     return (s, mse, best, cands) if return_candidates else (s, mse, best)
 
 
@@ -293,8 +304,8 @@ def pack_int3(W: torch.Tensor, s: torch.Tensor | None = None, out=None, stream=N
 
 def w3a16_gemm(X: torch.Tensor, planes: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,
                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Y = X deq(Wq)^T over the 3-bit planes of ``pack_int3``, fp16 [M, N],
-    M <= 16."""
+    """Y = X deq(Wq)^T over the 3-bit planes of ``pack_int3``, fp16 [M, N]
+    (decode kernel for M <= 16, tensor cores above)."""
     _dev(X, torch.float16, "X")
     _dev(planes, torch.int32, "planes")
     _dev(scales, torch.float16, "scales")

@@ -352,12 +352,16 @@ size_t awq_search_workspace_size(int64_t N, int64_t K, int64_t T, int n_alpha) {
     return search_ws(N, K, T, n_alpha).total;
 }
 
-awq_status awq_search_scale(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
-                            const uint16_t* Xcal, int64_t T, int64_t ldx, const double* mean_abs,
-                            const double* alphas, int n_alpha, int group, float* s_out,
-                            double* mse_out, int32_t* best_idx, float* s_alpha_out,
-                            void* workspace, size_t ws_bytes, awq_stream_t stream) {
-    const CallRange range("awq_search_scale");
+}  // extern "C"
+
+namespace {
+
+// awq_search_scale and its 3-bit form: levels 0..qmax.
+awq_status search_impl(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, const uint16_t* Xcal,
+                       int64_t T, int64_t ldx, const double* mean_abs, const double* alphas,
+                       int n_alpha, int group, float* s_out, double* mse_out, int32_t* best_idx,
+                       float* s_alpha_out, void* workspace, size_t ws_bytes, awq_stream_t stream,
+                       float qmax) {
     if (N <= 0 || K <= 0 || T <= 0 || n_alpha < 1 || n_alpha > AWQ_MAX_ALPHAS)
         return fail(AWQ_ERR_INVALID_ARG, "search_scale: sizes must be positive, 1 <= n_alpha <= 64");
     if (!W || !Xcal || !mean_abs || !alphas || !s_out || !best_idx)
@@ -407,11 +411,37 @@ awq_status awq_search_scale(const uint16_t* W, int64_t N, int64_t K, int64_t ldw
     p.inv_s_alpha = inv_s;
     p.partials = partials;
     p.status = d->status;
+    p.qmax = qmax;
     e = awq::launch_tc_search(map, p, d->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e);
     e = awq::launch_search_finalize(partials, n_alpha, (int64_t)p.n_tiles * p.t_tiles * 4, T, N, K,
                                     s_alpha, mse, best_idx, s_out, st);
     return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+awq_status awq_search_scale(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                            const uint16_t* Xcal, int64_t T, int64_t ldx, const double* mean_abs,
+                            const double* alphas, int n_alpha, int group, float* s_out,
+                            double* mse_out, int32_t* best_idx, float* s_alpha_out,
+                            void* workspace, size_t ws_bytes, awq_stream_t stream) {
+    const CallRange range("awq_search_scale");
+    return search_impl(W, N, K, ldw, Xcal, T, ldx, mean_abs, alphas, n_alpha, group, s_out,
+                       mse_out, best_idx, s_alpha_out, workspace, ws_bytes, stream, 15.0f);
+}
+
+awq_status awq_search_scale_int3(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                                 const uint16_t* Xcal, int64_t T, int64_t ldx,
+                                 const double* mean_abs, const double* alphas, int n_alpha,
+                                 int group, float* s_out, double* mse_out, int32_t* best_idx,
+                                 float* s_alpha_out, void* workspace, size_t ws_bytes,
+                                 awq_stream_t stream) {
+    const CallRange range("awq_search_scale_int3");
+    return search_impl(W, N, K, ldw, Xcal, T, ldx, mean_abs, alphas, n_alpha, group, s_out,
+                       mse_out, best_idx, s_alpha_out, workspace, ws_bytes, stream, 7.0f);
 }
 
 // Tokens of the transposed copy: T rounded up to a whole 64-token TMA box.
@@ -470,12 +500,14 @@ size_t awq_search_gram_workspace_size(int64_t N, int64_t K, int n_alpha) {
     return search_ws(N, K, K, n_alpha).total;
 }
 
-awq_status awq_search_scale_gram(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
-                                 const uint16_t* G, const double* mean_abs, const double* alphas,
-                                 int n_alpha, int group, float* s_out, double* mse_out,
-                                 int32_t* best_idx, float* s_alpha_out, void* workspace,
-                                 size_t ws_bytes, awq_stream_t stream) {
-    const CallRange range("awq_search_scale_gram");
+}  // extern "C"
+
+namespace {
+
+awq_status search_gram_impl(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, const uint16_t* G,
+                            const double* mean_abs, const double* alphas, int n_alpha, int group,
+                            float* s_out, double* mse_out, int32_t* best_idx, float* s_alpha_out,
+                            void* workspace, size_t ws_bytes, awq_stream_t stream, float qmax) {
     if (N <= 0 || K <= 0 || n_alpha < 1 || n_alpha > AWQ_MAX_ALPHAS)
         return fail(AWQ_ERR_INVALID_ARG, "search_scale_gram: sizes must be positive, 1 <= n_alpha <= 64");
     if (!W || !G || !mean_abs || !alphas || !s_out || !best_idx)
@@ -523,12 +555,37 @@ awq_status awq_search_scale_gram(const uint16_t* W, int64_t N, int64_t K, int64_
     p.inv_s_alpha = inv_s;
     p.partials = partials;
     p.status = d->status;
+    p.qmax = qmax;
     e = awq::launch_tc_gram_search(map, p, d->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e);
     // G already carries the 1/T of the mean: divide the sums by N only
     e = awq::launch_search_finalize(partials, n_alpha, (int64_t)p.n_tiles * p.t_tiles * 4, 1, N, K,
                                     s_alpha, mse, best_idx, s_out, st);
     return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+awq_status awq_search_scale_gram(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                                 const uint16_t* G, const double* mean_abs, const double* alphas,
+                                 int n_alpha, int group, float* s_out, double* mse_out,
+                                 int32_t* best_idx, float* s_alpha_out, void* workspace,
+                                 size_t ws_bytes, awq_stream_t stream) {
+    const CallRange range("awq_search_scale_gram");
+    return search_gram_impl(W, N, K, ldw, G, mean_abs, alphas, n_alpha, group, s_out, mse_out,
+                            best_idx, s_alpha_out, workspace, ws_bytes, stream, 15.0f);
+}
+
+awq_status awq_search_scale_gram_int3(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                                      const uint16_t* G, const double* mean_abs,
+                                      const double* alphas, int n_alpha, int group, float* s_out,
+                                      double* mse_out, int32_t* best_idx, float* s_alpha_out,
+                                      void* workspace, size_t ws_bytes, awq_stream_t stream) {
+    const CallRange range("awq_search_scale_gram_int3");
+    return search_gram_impl(W, N, K, ldw, G, mean_abs, alphas, n_alpha, group, s_out, mse_out,
+                            best_idx, s_alpha_out, workspace, ws_bytes, stream, 7.0f);
 }
 
 awq_status awq_pack_int4(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, const float* s,
@@ -559,19 +616,44 @@ awq_status w3a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
     if (M == 0 || N == 0) return AWQ_OK;
     if (!X || !planes || !scales || !zeros || !Y)
         return fail(AWQ_ERR_INVALID_ARG, "w3a16_gemm: null pointer");
-    if (M > 16 || group != AWQ_GROUP || K <= 0 || K % AWQ_GROUP || N % 8 || ldx < K || ldx % 8 ||
-        ldy < N)
-        return fail(AWQ_ERR_SHAPE, "w3a16_gemm: need M <= 16, group 128, K % 128 == 0, N % 8 == 0, ldx >= K, ldx % 8 == 0, ldy >= N");
-    if (N > (1LL << 30) || K > (1LL << 30)) return fail(AWQ_ERR_SHAPE, "w3a16_gemm: size too large");
+    if (group != AWQ_GROUP || K <= 0 || K % AWQ_GROUP || N % 8 || ldx < K || ldx % 8 || ldy < N)
+        return fail(AWQ_ERR_SHAPE, "w3a16_gemm: need group 128, K % 128 == 0, N % 8 == 0, ldx >= K, ldx % 8 == 0, ldy >= N");
+    if (M > (1LL << 30) || N > (1LL << 30) || K > (1LL << 30))
+        return fail(AWQ_ERR_SHAPE, "w3a16_gemm: size too large");
     if (!aligned16(X) || (reinterpret_cast<uintptr_t>(planes) & 3u) ||
-        (reinterpret_cast<uintptr_t>(Y) & 1u) || (reinterpret_cast<uintptr_t>(scales) & 1u) ||
-        (reinterpret_cast<uintptr_t>(zeros) & 1u))
-        return fail(AWQ_ERR_ALIGN, "w3a16_gemm: X must be 16-byte aligned, planes 4-byte");
+        (M > 16 && !aligned16(planes)) || (reinterpret_cast<uintptr_t>(Y) & 1u) ||
+        (reinterpret_cast<uintptr_t>(scales) & 1u) || (reinterpret_cast<uintptr_t>(zeros) & 1u))
+        return fail(AWQ_ERR_ALIGN, "w3a16_gemm: X must be 16-byte aligned, planes 4-byte (16-byte for M > 16)");
     DevInfo* d = nullptr;
     awq_status st_ = device_info(&d);
     if (st_) return st_;
-    cudaError_t e = awq::launch_gemv_w3a16(X, ldx, (int)M, planes, scales, zeros, N, K, Y, ldy,
-                                           d->num_sms, (cudaStream_t)stream);
+    cudaError_t e;
+    if (M <= 16) {
+        e = awq::launch_gemv_w3a16(X, ldx, (int)M, planes, scales, zeros, N, K, Y, ldy,
+                                   d->num_sms, (cudaStream_t)stream);
+    } else {
+        // prefill: the tcgen05 GEMM with a producer that rebuilds fp16 levels
+        // from the planes (no split of K, so no workspace)
+        CUtensorMap map;
+        awq_status s = make_act_map(&map, X, M, K, ldx);
+        if (s) return s;
+        awq::TcParams p = {};
+        p.N = (int)N;
+        p.K = (int)K;
+        p.G = (int)(K / AWQ_GROUP);
+        p.rows_tok = (int)M;
+        p.n_tiles = (int)((N + awq::kTcRows - 1) / awq::kTcRows);
+        p.t_tiles = (int)((M + awq::kGemmTokensPerItem - 1) / awq::kGemmTokensPerItem);
+        p.k_splits = 1;
+        p.n_items = p.n_tiles * p.t_tiles;
+        p.planes = planes;
+        p.scales = scales;
+        p.zeros = zeros;
+        p.Y = Y;
+        p.ldy = ldy;
+        p.status = d->status;
+        e = awq::launch_tc_gemm3(map, p, d->num_sms, (cudaStream_t)stream);
+    }
     return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
 }
 

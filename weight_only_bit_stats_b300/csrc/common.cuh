@@ -144,11 +144,14 @@ struct GroupQuant {
     bool finite;    // false when the fp16 scale overflowed
 };
 
-// Group parameters from the group's min and max (already reduced).
-__device__ __forceinline__ GroupQuant group_quant_from_range(float lo, float hi) {
+// Group parameters from the group's min and max (already reduced), for
+// levels 0..qmax (15 at 4 bits, 7 at 3 bits): d = fp32(range / qmax) is one
+// IEEE division whatever qmax is.
+__device__ __forceinline__ GroupQuant group_quant_from_range(float lo, float hi,
+                                                            float qmax = 15.0f) {
     GroupQuant g;
     float range = __fsub_rn(hi, lo);
-    float d = __fdiv_rn(range, 15.0f);
+    float d = __fdiv_rn(range, qmax);
     d = fmaxf(d, 6.103515625e-05f);              // 2^-14, least normal fp16
     g.scale_h = __float2half_rn(d);
     g.scale = __half2float(g.scale_h);
@@ -156,7 +159,7 @@ __device__ __forceinline__ GroupQuant group_quant_from_range(float lo, float hi)
     g.rcp = __frcp_rn(g.scale);
     // the zero-point is an integer level: -0 and negatives clamp to +0
     float z = rint_quot(-lo, g.scale, g.rcp);
-    g.zf = z > 0.0f ? fminf(z, 15.0f) : 0.0f;
+    g.zf = z > 0.0f ? fminf(z, qmax) : 0.0f;
     return g;
 }
 

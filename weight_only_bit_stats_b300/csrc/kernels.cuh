@@ -105,6 +105,10 @@ struct TcParams {
     // X^T X: fp16 out [N][rows_tok] (= [K][K]) scaled by inv_t
     uint16_t* gout;
     float inv_t;
+    // search: top quantisation level (15 at 4 bits, 7 at 3 bits)
+    float qmax;
+    // 3-bit GEMM: bit planes [N][K/32][3] in place of qw
+    const uint32_t* planes;
 };
 constexpr int kTcRows = 128;          // weight rows per tile (UMMA M)
 constexpr int kTcTokens = 256;        // tokens per accumulator slot (UMMA N)
@@ -129,6 +133,10 @@ cudaError_t launch_tc_xtx(const CUtensorMap& mapB, const CUtensorMap& mapA, cons
 // rows); partials as the direct search, already divided by T.
 cudaError_t launch_tc_gram_search(const CUtensorMap& mapG, const TcParams& p, int num_sms,
                                   cudaStream_t st);
+// W3A16 GEMM for M > 16 over the 3-bit planes (p.planes, p.scales, p.zeros);
+// no split-K (k_splits must be 1).
+cudaError_t launch_tc_gemm3(const CUtensorMap& mapX, const TcParams& p, int num_sms,
+                            cudaStream_t st);
 // X^T [K][T_pad] (zero columns past T) from X [T][K] (leading dimension ldx).
 cudaError_t launch_transpose_x(const uint16_t* X, int64_t T, int64_t K, int64_t ldx,
                                uint16_t* Xt, int64_t T_pad, cudaStream_t st);

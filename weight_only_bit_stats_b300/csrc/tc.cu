@@ -41,7 +41,7 @@
 namespace awq {
 namespace {
 
-enum { kModeGemm = 0, kModeSearch = 1, kModeXtX = 2, kModeGram = 3 };
+enum { kModeGemm = 0, kModeSearch = 1, kModeXtX = 2, kModeGram = 3, kModeGemm3 = 4 };
 
 constexpr int kNA = 2;                            // A (weight) stages
 constexpr int kNB = 2;                            // B (activation) stages
@@ -53,11 +53,17 @@ constexpr int kTmemCols = 512;
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpTmem = 2, kWarpEpi0 = 4, kWarpProd0 = 8;
 
+// The two W4A16 / W3A16 GEMM modes share everything but the producer.
+template <int MODE>
+constexpr bool is_gemm() {
+    return MODE == kModeGemm || MODE == kModeGemm3;
+}
+
 template <int MODE>
 struct Cfg {
-    static constexpr int kProdWarps = MODE == kModeGemm ? 4 : (MODE == kModeXtX ? 0 : 16);
+    static constexpr int kProdWarps = is_gemm<MODE>() ? 4 : (MODE == kModeXtX ? 0 : 16);
     static constexpr int kThreads = (kWarpProd0 + kProdWarps) * 32;
-    static constexpr int kHalves = MODE == kModeGemm ? 1 : 2;   // accumulators per item
+    static constexpr int kHalves = is_gemm<MODE>() ? 1 : 2;     // accumulators per item
 };
 
 // Group parameters the Gram-search producer exports for the epilogue: for
@@ -95,7 +101,7 @@ struct Item {
 template <int MODE>
 __device__ __forceinline__ Item decode_item(int item, const TcParams& p) {
     Item it;
-    if (MODE == kModeGemm) {
+    if (is_gemm<MODE>()) {
         // token tiles in bands of up to 8 (2048 tokens): within a band,
         // consecutive CTAs share a weight tile (the band's token tiles of one
         // weight tile run together) and the weight tiles go round, so the
@@ -329,7 +335,7 @@ __device__ void role_epilogue(const TcParams& p, SmemCtl* ctl, const GramParams*
                             float v8[8];
                             tmem_ld8(taddr + c * 32 + 8 * j, v8);
                             acc += gram_dot8(p, s_a, is_a, wr, valid, col + 8 * j, scale, rcp, -zf,
-                                             15.0f - zf, v8);
+                                             p.qmax - zf, v8);
                         }
                         if (valid) dsum += (double)acc;
                     }
@@ -337,7 +343,7 @@ __device__ void role_epilogue(const TcParams& p, SmemCtl* ctl, const GramParams*
                 }
                 float v[32];
                 tmem_ld32(taddr + c * 32, v);
-                if (MODE == kModeGemm) {
+                if (is_gemm<MODE>()) {
                     if (n < p.N) {
                         if (p.k_splits == 1) {
 #pragma unroll
@@ -520,6 +526,108 @@ __device__ void role_prod_gemm(const TcParams& p, uint8_t* As, SmemCtl* ctl, int
     }
 }
 
+// ---- role: W3A16 GEMM producer (3-bit planes -> fp16 (q - z) * scale) ----
+// Rotating plane p of a 32-level block right by (i - p) mod 32 puts bit i of
+// the plane at bit p and bit i + 16 at bit 16 + p; OR-ing the three under
+// the mantissa of fp16 1024 gives the exact pair (1024 + q_i, 1024 + q_{i+16}),
+// and one HSUB2 the exact (q - z) pair.  Times the fp16 scale (HMUL2) it is
+// rounded once to fp16, as in the 4-bit producer.  The pairs (i, i+16) of
+// i = 8m .. 8m + 7 are then gathered (PRMT) into the 16-byte chunks of levels
+// 8m .. 8m + 7 (low halves) and 16 + 8m .. (high halves).
+__device__ __forceinline__ uint32_t rotr32(uint32_t w, uint32_t n) { return __funnelshift_r(w, w, n); }
+
+__device__ __forceinline__ void dequant_block3(uint32_t p0, uint32_t p1, uint32_t p2,
+                                               __half2 z1024, __half2 sc, uint4 (&o)[4]) {
+    uint32_t pr[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        uint32_t v = lop3_and_or(rotr32(p0, (uint32_t)i & 31u), 0x00010001u, 0x64006400u);
+        v = lop3_and_or(rotr32(p1, (uint32_t)(i - 1) & 31u), 0x00020002u, v);
+        v = lop3_and_or(rotr32(p2, (uint32_t)(i - 2) & 31u), 0x00040004u, v);
+        pr[i] = h2u(__hmul2(__hsub2(u2h(v), z1024), sc));
+    }
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        o[m] = make_uint4(prmt(pr[8 * m], pr[8 * m + 1], 0x5410), prmt(pr[8 * m + 2], pr[8 * m + 3], 0x5410),
+                          prmt(pr[8 * m + 4], pr[8 * m + 5], 0x5410), prmt(pr[8 * m + 6], pr[8 * m + 7], 0x5410));
+        o[m + 2] = make_uint4(prmt(pr[8 * m], pr[8 * m + 1], 0x7632), prmt(pr[8 * m + 2], pr[8 * m + 3], 0x7632),
+                              prmt(pr[8 * m + 4], pr[8 * m + 5], 0x7632), prmt(pr[8 * m + 6], pr[8 * m + 7], 0x7632));
+    }
+}
+
+__device__ void role_prod_gemm3(const TcParams& p, uint8_t* As, SmemCtl* ctl, int r, int lane) {
+    volatile int* abort = &ctl->abort;
+    const int64_t wstride = p.K / 32 * 3;                // plane words per row
+    uint32_t a_iter = 0;
+    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+        const Item it = decode_item<kModeGemm3>(item, p);
+        const int64_t n = (int64_t)it.n_tile * kTcRows + r;
+        const bool valid = n < p.N;
+        const uint4* prow = reinterpret_cast<const uint4*>(p.planes + (valid ? n : 0) * wstride);
+        const uint16_t* srow = p.scales + (valid ? n : 0) * p.G;
+        const uint16_t* zrow = p.zeros + (valid ? n : 0) * p.G;
+        uint4 cur[3];
+        uint16_t csc = 0, cze = 0;
+        if (valid) {
+#pragma unroll
+            for (int j = 0; j < 3; ++j) cur[j] = __ldg(prow + (int64_t)it.g0 * 3 + j);
+            csc = __ldg(srow + it.g0);
+            cze = __ldg(zrow + it.g0);
+            for (int g = it.g0 + 2; g < it.g1 && g < it.g0 + kProdPrefetch; ++g)
+                prefetch_l2(prow + (int64_t)g * 3);
+        }
+        for (int g = it.g0; g < it.g1; ++g) {
+            uint4 nxt[3];
+            uint16_t nsc = 0, nze = 0;
+            if (valid && g + kProdPrefetch < it.g1) prefetch_l2(prow + (int64_t)(g + kProdPrefetch) * 3);
+            if (valid && g + 1 < it.g1) {
+#pragma unroll
+                for (int j = 0; j < 3; ++j) nxt[j] = __ldg(prow + (int64_t)(g + 1) * 3 + j);
+                nsc = __ldg(srow + g + 1);
+                nze = __ldg(zrow + g + 1);
+            }
+            const int st = a_iter % kNA;
+            if (!mbar_wait(&ctl->a_empty[st], ((a_iter / kNA) & 1u) ^ 1u, abort, p.status)) return;
+            uint8_t* tile = As + st * kAStage;
+            if (valid) {
+                const __half2 z1024 =
+                    __half2half2(__hadd(__float2half_rn(1024.0f), __ushort_as_half(cze)));
+                const __half2 sc = __half2half2(__ushort_as_half(csc));
+                const uint32_t w[12] = {cur[0].x, cur[0].y, cur[0].z, cur[0].w, cur[1].x, cur[1].y,
+                                        cur[1].z, cur[1].w, cur[2].x, cur[2].y, cur[2].z, cur[2].w};
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {            // 32-level blocks of the group
+                    uint4 o[4];
+                    dequant_block3(w[3 * b], w[3 * b + 1], w[3 * b + 2], z1024, sc, o);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const int k = 32 * b + 8 * m;    // 0..120 within the group
+                        *reinterpret_cast<uint4*>(tile + (k >> 6) * kASub + sw128_offset(r, k & 63)) =
+                            o[m];
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int k = j * 8;
+                    *reinterpret_cast<uint4*>(tile + (k >> 6) * kASub + sw128_offset(r, k & 63)) =
+                        make_uint4(0, 0, 0, 0);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->a_full[st]);
+            ++a_iter;
+            if (valid && g + 1 < it.g1) {
+#pragma unroll
+                for (int j = 0; j < 3; ++j) cur[j] = nxt[j];
+                csc = nsc;
+                cze = nze;
+            }
+        }
+    }
+}
+
 // ---- role: search producer (fake-quantise W diag(s), residual E in fp16) ----
 // Four lanes hold one row of the group: lane c the 16-byte chunks c and c + 4
 // of both 64-channel sub-tiles (channels 8c..8c+7, 32+8c.., 64+8c..,
@@ -609,14 +717,14 @@ __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, G
                 lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
                 hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
             }
-            const GroupQuant gq = group_quant_from_range(lo, hi);
+            const GroupQuant gq = group_quant_from_range(lo, hi, p.qmax);
             bad |= !gq.finite;
             if (GRAM && c == 0 && g >= g_par && g < g_par + 4) {
                 gp->scale[g - g_par][r] = gq.scale;
                 gp->rcp[g - g_par][r] = gq.rcp;
                 gp->zf[g - g_par][r] = gq.zf;
             }
-            const float neg_z = -gq.zf, top_z = 15.0f - gq.zf;
+            const float neg_z = -gq.zf, top_z = p.qmax - gq.zf;
             const int st = a_iter % kNA;
             if (!mbar_wait(&ctl->a_empty[st], ((a_iter / kNA) & 1u) ^ 1u, abort, p.status)) return;
             uint8_t* tile = As + st * kAStage;
@@ -709,6 +817,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     } else if (warp >= kWarpProd0) {
         if constexpr (MODE == kModeGemm)
             role_prod_gemm(p, As, ctl, (warp - kWarpProd0) * 32 + lane, lane);
+        else if constexpr (MODE == kModeGemm3)
+            role_prod_gemm3(p, As, ctl, (warp - kWarpProd0) * 32 + lane, lane);
         else if constexpr (MODE == kModeSearch)
             role_prod_search<Cfg<MODE>::kProdWarps, false>(p, As, ctl, gpar, warp - kWarpProd0,
                                                            lane);
@@ -768,6 +878,10 @@ cudaError_t launch_tc_gemm(const CUtensorMap& mapX, const TcParams& p, int num_s
 cudaError_t launch_tc_search(const CUtensorMap& mapX, const TcParams& p, int num_sms,
                              cudaStream_t st) {
     return launch_tc<kModeSearch>(mapX, mapX, p, num_sms, st);
+}
+cudaError_t launch_tc_gemm3(const CUtensorMap& mapX, const TcParams& p, int num_sms,
+                            cudaStream_t st) {
+    return launch_tc<kModeGemm3>(mapX, mapX, p, num_sms, st);
 }
 cudaError_t launch_tc_xtx(const CUtensorMap& mapB, const CUtensorMap& mapA, const TcParams& p,
                           int num_sms, cudaStream_t st) {
