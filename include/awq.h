@@ -339,6 +339,26 @@ awq_status w4a16_gemm_repacked(const uint16_t* X, int64_t M, int64_t K, int64_t 
                                const float* inv_s, const void* tiles, int64_t N, int group,
                                uint16_t* Y, int64_t ldy, awq_stream_t stream);
 
+/* The same repack at 3 bits: tile (j, g) of awq_pack_int3's planes at byte
+ * (j * (K/128) + g) * 832:
+ *   bytes [0, 768): 16 rows x 48 bytes: row 16 j + r's plane words
+ *     12 g .. 12 g + 11 at 48 r (rows at or past N zero);
+ *   bytes [768, 832): scales and zero-points as in the 4-bit tile.
+ * planes 16-byte aligned; tiles >= awq_repack_int3_bytes(N, K) bytes. */
+size_t awq_repack_int3_bytes(int64_t N, int64_t K);
+awq_status awq_repack_int3(const uint32_t* planes, const uint16_t* scales, const uint16_t* zeros,
+                           int64_t N, int64_t K, int group, void* tiles, size_t tiles_bytes,
+                           awq_stream_t stream);
+
+/* Y = X deq(Wq)^T for 1 <= M <= 16 over the 3-bit tiles (the arithmetic of
+ * w3a16_gemm's tensor-core decode: exact fp16 (q - z) pairs from the planes,
+ * fp32 accumulation per group, the scale in fp32, fp16 out; AWQ page sixth
+ * paragraph: fewer bytes per weight, faster small-batch tokens).  Arguments
+ * as w4a16_gemm_repacked without inv_s.  M > 16 returns AWQ_ERR_SHAPE. */
+awq_status w3a16_gemm_repacked(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
+                               const void* tiles, int64_t N, int group, uint16_t* Y, int64_t ldy,
+                               awq_stream_t stream);
+
 /* Overlap of back-to-back decode matmuls (M <= 16).  Every decode launch
  * lets the next kernel in the stream start beside it (programmatic dependent
  * launch) and reads X / writes Y only after the previous kernel in the stream

@@ -54,6 +54,7 @@ def test_version_and_workspace_sizes(capi):
     assert capi.awq_repack_int4_bytes(12288, 4096) == 768 * 32 * 1088
     assert capi.awq_repack_int4_bytes(136, 384) == 9 * 3 * 1088
     assert capi.awq_repack_int4_bytes(16, 100) == 0
+    assert capi.awq_repack_int3_bytes(12288, 4096) == 768 * 32 * 832
     # Gram route: the transposed calibration copy (T padded to 64) and the
     # search workspace over K columns in place of T tokens
     assert capi.awq_gram_workspace_size(300, 1024) >= 1024 * 320 * 2
@@ -115,6 +116,9 @@ def test_host_argument_checks(capi):
                                     None) == 3
     assert capi.w4a16_gemm_repacked(base, 1, 128, 128, None, base + 8, 16, 128, base, 16,
                                     None) == 3
+    # 3-bit repack and repacked matmul: planes alignment, decode sizes only
+    assert capi.awq_repack_int3(base + 4, base, base, 16, 128, 128, base, 4096, None) == 3
+    assert capi.w3a16_gemm_repacked(base, 17, 128, 128, base, 16, 128, base, 16, None) == 2
     # Gram route: K % 128, misaligned G, missing workspace
     assert capi.awq_gram(base, 64, 100, 100, base, base, 1 << 20, None) == 2
     assert capi.awq_gram(base, 64, 128, 128, base + 2, base, 1 << 20, None) == 3

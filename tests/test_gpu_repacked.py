@@ -217,3 +217,78 @@ def test_repacked_empty_and_strided(wb, orc):
     big[:, :512] = dev(X)
     y = host(wb.w4a16_gemm_repacked(big[:, :512], tiles, 256))
     assert rel_err(y, orc.w4a16_gemm(X, rq, rs, rz)) <= GEMM_TOL
+
+
+# ------------------------------------------------------------- 3 bits ----
+
+TILE3 = 832
+
+
+def tiles3_from_definition(planes, sc, ze):
+    """The 3-bit tile layout from its definition: tile (j, g) at byte
+    (j G + g) 832; row r's plane words 12 g .. 12 g + 11 at 48 r; then the
+    scale and zero-point block of the 4-bit tile; rows past N zero."""
+    N, W3 = planes.shape
+    G = W3 // 12
+    S = (N + 15) // 16
+    pl = np.zeros((S * 16, W3), dtype=np.uint32)
+    s = np.zeros((S * 16, G), dtype=np.uint16)
+    z = np.zeros((S * 16, G), dtype=np.uint16)
+    pl[:N], s[:N], z[:N] = planes, sc, ze
+    pl = pl.reshape(S, 16, G, 12)
+    s = s.reshape(S, 16, G)
+    z = z.reshape(S, 16, G)
+    out = np.zeros((S, G, TILE3), dtype=np.uint8)
+    out[:, :, :768] = np.ascontiguousarray(pl.transpose(0, 2, 1, 3)).view(np.uint8).reshape(S, G, 768)
+    for r in range(8):
+        sz = np.stack([s[:, r], z[:, r], s[:, r + 8], z[:, r + 8]], axis=-1)
+        out[:, :, 768 + 8 * r:768 + 8 * r + 8] = sz.view(np.uint8).reshape(S, G, 8)
+    return out.reshape(-1)
+
+
+@pytest.mark.parametrize("N,K", [(8, 128), (136, 384), (520, 2304), (4096, 4096)])
+def test_repack3_layout_bit_exact(wb, orc, N, K):
+    W, _, _, _ = sg.layer_inputs(56, 0, N, K, 0)
+    rp, rs, rz = orc.pack_int3(W)
+    nbytes = wb.lib().awq_repack_int3_bytes(N, K)
+    assert nbytes == (N + 15) // 16 * (K // 128) * TILE3
+    tiles = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device="cuda")
+    wb.repack_int3(dev(rp.view(np.int32)), dev(rs.view(np.float16)), dev(rz.view(np.float16)),
+                   out=tiles)
+    assert np.array_equal(host(tiles), tiles3_from_definition(rp, rs, rz))
+
+
+def _check_repacked3(wb, orc, X, rp, rs, rz):
+    M, N = X.shape[0], rp.shape[0]
+    tiles = wb.repack_int3(dev(rp.view(np.int32)), dev(rs.view(np.float16)),
+                           dev(rz.view(np.float16)))
+    Y = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    wb.w3a16_gemm_repacked(dev(X), tiles, N, out=Y)
+    y = host(Y)
+    assert np.all(np.isfinite(y))
+    err = rel_err(y, orc.w3a16_gemm(X, rp, rs, rz))
+    assert err <= GEMM_TOL, err
+    return y, tiles
+
+
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 9, 16])
+@pytest.mark.parametrize("N,K", [(8, 256), (136, 384), (1024, 1024), (520, 2304), (2400, 1152)])
+def test_repacked3_decode_parity(wb, orc, M, N, K):
+    W, _, X, _ = sg.layer_inputs(57, 0, N, K, 0, M=M)
+    rp, rs, rz = orc.pack_int3(W)
+    _check_repacked3(wb, orc, X, rp, rs, rz)
+
+
+def test_repacked3_llama7b_qkv_and_long_k(wb, orc):
+    """The LLaMA-7B qkv projection at M = 1 over the GPU's own 3-bit pack,
+    and M = 16 with K = 13824, where the activations do not fit in shared
+    memory and are read through L1."""
+    W, _, X, _ = sg.layer_inputs(0, 0, 12288, 4096, 0, M=1)
+    pl, sc, ze = wb.pack_int3(dev(W))
+    rp, rs, rz = orc.pack_int3(W)
+    assert np.array_equal(host(pl).view(np.uint32), rp)
+    _check_repacked3(wb, orc, X, rp, rs, rz)
+    W, _, X, _ = sg.layer_inputs(58, 0, 136, 13824, 0, M=16)
+    rp, rs, rz = orc.pack_int3(W)
+    _check_repacked3(wb, orc, X, rp, rs, rz)
+    wb.sync_status()

@@ -25,7 +25,8 @@ import torch
 
 __all__ = ["AwqError", "lib", "act_stats", "act_mean", "candidate_scales", "search_scale",
            "pack_int4", "pack_int3", "w4a16_gemm", "w3a16_gemm", "w4a16_gemm_scaled",
-           "repack_int4", "w4a16_gemm_repacked", "gram", "search_scale_gram",
+           "repack_int4", "w4a16_gemm_repacked", "repack_int3", "w3a16_gemm_repacked",
+           "gram", "search_scale_gram",
            "set_weight_prefetch",
            "sync_status",
            "ALPHA_GRID",
@@ -72,6 +73,9 @@ SIGNATURES = (
                                  _sz, _p]),
     ("w4a16_gemm_scaled_workspace_size", _sz, [_i64, _i64, _i64]),
     ("awq_repack_int4_bytes", _sz, [_i64, _i64]),
+    ("awq_repack_int3_bytes", _sz, [_i64, _i64]),
+    ("awq_repack_int3", _int, [_p, _p, _p, _i64, _i64, _int, _p, _sz, _p]),
+    ("w3a16_gemm_repacked", _int, [_p, _i64, _i64, _i64, _p, _i64, _int, _p, _i64, _p]),
     ("awq_gram_workspace_size", _sz, [_i64, _i64]),
     ("awq_gram", _int, [_p, _i64, _i64, _i64, _p, _p, _sz, _p]),
     ("awq_search_gram_workspace_size", _sz, [_i64, _i64, _int]),
@@ -373,6 +377,38 @@ def w4a16_gemm_repacked(X: torch.Tensor, tiles: torch.Tensor, N: int,
                                      inv_s.data_ptr() if inv_s is not None else None,
                                      tiles.data_ptr(), N, GROUP, Y.data_ptr(), _ld(Y),
                                      _stream(stream)), "w4a16_gemm_repacked")
+    return Y
+
+
+def repack_int3(planes: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The 3-bit planes regrouped into contiguous decode tiles (uint8
+    [awq_repack_int3_bytes(N, K)]), one 832-byte tile per 16 rows x 128
+    input channels."""
+    _dev(planes, torch.int32, "planes")
+    _dev(scales, torch.float16, "scales")
+    _dev(zeros, torch.float16, "zeros")
+    N, W3 = planes.shape
+    K = W3 // 3 * 32
+    nbytes = lib().awq_repack_int3_bytes(N, K)
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=planes.device)
+    _dev(out, torch.uint8, "tiles")
+    _check(lib().awq_repack_int3(planes.data_ptr(), scales.data_ptr(), zeros.data_ptr(), N, K,
+                                 GROUP, out.data_ptr(), out.numel(), _stream(stream)),
+           "awq_repack_int3")
+    return out
+
+
+def w3a16_gemm_repacked(X: torch.Tensor, tiles: torch.Tensor, N: int,
+                        out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y = X deq(Wq)^T over the 3-bit decode tiles of an [N, K] weight, M <= 16."""
+    _dev(X, torch.float16, "X")
+    _dev(tiles, torch.uint8, "tiles")
+    M, K = X.shape
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=X.device)
+    _check(lib().w3a16_gemm_repacked(X.data_ptr(), M, K, _ld(X), tiles.data_ptr(), N, GROUP,
+                                     Y.data_ptr(), _ld(Y), _stream(stream)), "w3a16_gemm_repacked")
     return Y
 
 

@@ -871,7 +871,59 @@ awq_status w4a16_gemm_repacked(const uint16_t* X, int64_t M, int64_t K, int64_t 
     if (s) return s;
     awq::TileParams p = {X, ldx, (int)M, static_cast<const uint8_t*>(tiles), N,
                          (int)(K / AWQ_GROUP), Y, ldy, d->status,
-                         g_early_weights.load(std::memory_order_relaxed), inv_s};
+                         g_early_weights.load(std::memory_order_relaxed), inv_s, 4};
+    cudaError_t e = awq::launch_gemv_tiles(p, d->num_sms, (cudaStream_t)stream);
+    return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
+}
+
+size_t awq_repack_int3_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0 || K % AWQ_GROUP) return 0;
+    return (size_t)((N + 15) / 16) * (size_t)(K / AWQ_GROUP) * (size_t)awq::kTile3Bytes;
+}
+
+awq_status awq_repack_int3(const uint32_t* planes, const uint16_t* scales, const uint16_t* zeros,
+                           int64_t N, int64_t K, int group, void* tiles, size_t tiles_bytes,
+                           awq_stream_t stream) {
+    const CallRange range("awq_repack_int3");
+    if (N < 0 || K < 0) return fail(AWQ_ERR_INVALID_ARG, "repack_int3: negative size");
+    if (N == 0 || K == 0) return AWQ_OK;
+    if (!planes || !scales || !zeros || !tiles)
+        return fail(AWQ_ERR_INVALID_ARG, "repack_int3: null pointer");
+    if (group != AWQ_GROUP || K % AWQ_GROUP || N > (1LL << 30) || K > (1LL << 30))
+        return fail(AWQ_ERR_SHAPE, "repack_int3: need group 128, K % 128 == 0");
+    if (!aligned16(planes) || !aligned16(tiles) || (reinterpret_cast<uintptr_t>(scales) & 1u) ||
+        (reinterpret_cast<uintptr_t>(zeros) & 1u))
+        return fail(AWQ_ERR_ALIGN, "repack_int3: planes and tiles must be 16-byte aligned");
+    if (tiles_bytes < awq_repack_int3_bytes(N, K))
+        return fail(AWQ_ERR_WORKSPACE, "repack_int3: tiles buffer smaller than awq_repack_int3_bytes(N, K)");
+    DevInfo* d = nullptr;
+    awq_status s = device_info(&d);
+    if (s) return s;
+    cudaError_t e = awq::launch_repack_int3(planes, scales, zeros, N, K, tiles, d->num_sms,
+                                            (cudaStream_t)stream);
+    return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
+}
+
+awq_status w3a16_gemm_repacked(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
+                               const void* tiles, int64_t N, int group, uint16_t* Y, int64_t ldy,
+                               awq_stream_t stream) {
+    const CallRange range("w3a16_gemm_repacked");
+    if (M < 0 || N < 0 || K < 0) return fail(AWQ_ERR_INVALID_ARG, "w3a16_gemm_repacked: negative size");
+    if (M == 0 || N == 0) return AWQ_OK;
+    if (!X || !tiles || !Y) return fail(AWQ_ERR_INVALID_ARG, "w3a16_gemm_repacked: null pointer");
+    if (M > 16 || group != AWQ_GROUP || K <= 0 || K % AWQ_GROUP || N % 8 || ldx < K || ldx % 8 ||
+        ldy < N)
+        return fail(AWQ_ERR_SHAPE, "w3a16_gemm_repacked: need M <= 16, group 128, K % 128 == 0, N % 8 == 0, ldx >= K, ldx % 8 == 0, ldy >= N");
+    if (N > (1LL << 30) || K > (1LL << 30))
+        return fail(AWQ_ERR_SHAPE, "w3a16_gemm_repacked: size too large");
+    if (!aligned16(X) || !aligned16(tiles) || (reinterpret_cast<uintptr_t>(Y) & 1u))
+        return fail(AWQ_ERR_ALIGN, "w3a16_gemm_repacked: X and tiles must be 16-byte aligned");
+    DevInfo* d = nullptr;
+    awq_status s = device_info(&d);
+    if (s) return s;
+    awq::TileParams p = {X, ldx, (int)M, static_cast<const uint8_t*>(tiles), N,
+                         (int)(K / AWQ_GROUP), Y, ldy, d->status,
+                         g_early_weights.load(std::memory_order_relaxed), nullptr, 3};
     cudaError_t e = awq::launch_gemv_tiles(p, d->num_sms, (cudaStream_t)stream);
     return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
 }

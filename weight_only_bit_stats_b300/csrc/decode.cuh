@@ -345,5 +345,120 @@ __device__ __forceinline__ void stage_x_folded(uint8_t* xsm, uint8_t* bs, const 
     }
 }
 
+// ---------------------------------------------------------------------------
+// 3-bit planes (three words per 32 levels: word p holds bit p of level i at
+// bit i).  Rotating plane p right by (i - p) mod 32 puts bit i at bit p and
+// bit i + 16 at bit 16 + p; OR-ing the three under the mantissa of fp16 1024
+// gives the exact pair (1024 + q_i, 1024 + q_{i+16}), and an HSUB2 of
+// (1024 + z) the exact pair (q_i - z, q_{i+16} - z).  Lane t of a row builds
+// the pairs i = t, t + 4, t + 8, t + 12 of a block: its A fragments of two
+// m16n8k16 MMAs, whose k order is a permutation of the block's levels; the
+// activations are staged in the matching order (stage_x3).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t rotr32(uint32_t w, uint32_t n) { return __funnelshift_r(w, w, n); }
+
+__device__ __forceinline__ uint32_t pair3_mz(uint32_t p0, uint32_t p1, uint32_t p2, uint32_t r0,
+                                             uint32_t r1, uint32_t r2, __half2 z1024) {
+    uint32_t v = lop3_and_or(rotr32(p0, r0), 0x00010001u, 0x64006400u);
+    v = lop3_and_or(rotr32(p1, r1), 0x00020002u, v);
+    v = lop3_and_or(rotr32(p2, r2), 0x00040004u, v);
+    return h2_as_u32(__hsub2(u32_as_h2(v), z1024));
+}
+
+// Per token a row of K * 2 + 64 bytes; block j's 64 bytes hold, for lane
+// column t = 0..3, the 16 bytes x[32 j + t + {0, 16, 4, 20, 8, 24, 12, 28}]
+// (lane t's B fragments of the block's two MMAs).
+__host__ __device__ constexpr int64_t dec_x3_row_bytes(int64_t K) { return K * 2 + 64; }
+
+// Stage the M x K activations in that order: one thread per (token, block)
+// loads the block's 64 bytes and writes its four 16-byte fragment groups.
+// Called by all nthreads threads, followed by a barrier.
+__device__ __forceinline__ void stage_x3(uint8_t* xsm, const uint16_t* X, int64_t ldx, int M,
+                                         int64_t K, int tid, int nthreads) {
+    const int64_t xrow = dec_x3_row_bytes(K);
+    const int nblk = (int)(K / 32);
+    for (int idx = tid; idx < M * nblk; idx += nthreads) {
+        const int m = idx / nblk, j = idx - m * nblk;
+        const uint4* src = reinterpret_cast<const uint4*>(X + (int64_t)m * ldx + 32 * (int64_t)j);
+        uint32_t w[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 v = __ldg(src + q);
+            w[4 * q] = v.x;
+            w[4 * q + 1] = v.y;
+            w[4 * q + 2] = v.z;
+            w[4 * q + 3] = v.w;
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            uint32_t o[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int lo = t + 4 * c, hi = lo + 16;     // levels of this pair
+                const uint32_t sel = ((lo & 1) ? 0x3232u : 0x1010u) & 0x00FFu;
+                const uint32_t selh = ((hi & 1) ? 0x7676u : 0x5454u) & 0xFF00u;
+                o[c] = prmt(w[lo >> 1], w[hi >> 1], sel | selh);
+            }
+            *reinterpret_cast<uint4*>(xsm + (int64_t)m * xrow + (int64_t)j * 64 + t * 16) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+// y += scale * (X_group (q - z)^T) for one group of the 3-bit tile rows g and
+// g + 8 (plane words A and B, 12 each), 2 (4 for NB = 2) MMAs per 32-level
+// block.  xs: the staged rows (XS), else the activations are read from X.
+template <int NB, bool XS>
+__device__ __forceinline__ void group_mma3(float (&y)[NB][4], uint2 sz, const uint32_t (&A)[12],
+                                           const uint32_t (&B)[12], const uint8_t* const (&xs)[NB],
+                                           const uint16_t* X, int64_t ldx, int M, int gi, int g,
+                                           int t) {
+    const __half h1024 = __float2half_rn(1024.0f);
+    const __half2 za = __half2half2(__hadd(h1024, __ushort_as_half((unsigned short)(sz.x >> 16))));
+    const __half2 zb = __half2half2(__hadd(h1024, __ushort_as_half((unsigned short)(sz.y >> 16))));
+    float c[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) c[nb][k] = 0.0f;
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+        uint32_t fa[4], fb[4];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            const uint32_t r0 = (uint32_t)(t + 4 * cc) & 31u, r1 = (uint32_t)(t + 4 * cc - 1) & 31u,
+                           r2 = (uint32_t)(t + 4 * cc - 2) & 31u;
+            fa[cc] = pair3_mz(A[3 * blk], A[3 * blk + 1], A[3 * blk + 2], r0, r1, r2, za);
+            fb[cc] = pair3_mz(B[3 * blk], B[3 * blk + 1], B[3 * blk + 2], r0, r1, r2, zb);
+        }
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            uint4 xb;
+            if constexpr (XS) {
+                xb = *reinterpret_cast<const uint4*>(xs[nb] + ((int64_t)gi * 4 + blk) * 64 + t * 16);
+            } else {
+                const int tok = min(g + 8 * nb, M - 1);
+                const uint16_t* xp = X + (int64_t)tok * ldx + (int64_t)gi * kGroup + 32 * blk + t;
+                uint32_t o[4];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    o[cc] = (uint32_t)__ldg(xp + 4 * cc) | ((uint32_t)__ldg(xp + 4 * cc + 16) << 16);
+                xb = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            mma16816(c[nb], fa[0], fb[0], fa[1], fb[1], xb.x, xb.y);
+            mma16816(c[nb], fa[2], fb[2], fa[3], fb[3], xb.z, xb.w);
+        }
+    }
+    const float sa = __half2float(__ushort_as_half((unsigned short)(sz.x & 0xFFFFu)));
+    const float sb = __half2float(__ushort_as_half((unsigned short)(sz.y & 0xFFFFu)));
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        y[nb][0] = fmaf(sa, c[nb][0], y[nb][0]);
+        y[nb][1] = fmaf(sa, c[nb][1], y[nb][1]);
+        y[nb][2] = fmaf(sb, c[nb][2], y[nb][2]);
+        y[nb][3] = fmaf(sb, c[nb][3], y[nb][3]);
+    }
+}
+
 }  // namespace dec
 }  // namespace awq

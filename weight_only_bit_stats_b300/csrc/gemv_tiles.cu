@@ -68,25 +68,32 @@ using namespace dec;
 #define AWQ_TILE_EARLY_STAGES 8
 #endif
 constexpr int kTilesPerStage = AWQ_TILES_PER_STAGE;
-constexpr int kTStageBytes = kTilesPerStage * kTileBytes;
 constexpr int kMaxTStages = 4;
-static_assert(kTileBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
+static_assert(kTileBytes % 16 == 0 && kTile3Bytes % 16 == 0,
+              "bulk copies move multiples of 16 bytes");
 
-template <int NB>
+template <int BITS>
+constexpr int tile_bytes() {
+    return BITS == 4 ? kTileBytes : kTile3Bytes;
+}
+
+template <int BITS, int NB>
 struct TileCfg {
+    static constexpr int kTile = tile_bytes<BITS>();
+    static constexpr int kStageBytes = kTilesPerStage * kTile;
     static constexpr int kWarps = NB == 1 ? AWQ_TILE_WARPS_NB1 : 8;
     static constexpr int kThreads = kWarps * 32;
     static constexpr int kStages = NB == 1 ? AWQ_TILE_STAGES_NB1 : AWQ_TILE_STAGES_NB2;
     static constexpr int kCols = 8 * NB;
     static constexpr int kSlots = 2 * kWarps;
-    static constexpr size_t kRingBytes = (size_t)kWarps * kStages * kTStageBytes;
+    static constexpr size_t kRingBytes = (size_t)kWarps * kStages * kStageBytes;
     static constexpr size_t kPartBytes = (size_t)kSlots * kDecRows * kCols * sizeof(float);
     static constexpr size_t kCtlBytes =
         (size_t)kWarps * kMaxTStages * 8 + (size_t)kWarps * 12 + 16;
     static constexpr size_t kSmem = 128 + kRingBytes + kPartBytes + kCtlBytes;
 };
 constexpr size_t kTileSmemMax = 232448;                 // per-block opt-in limit on sm_103
-static_assert(TileCfg<1>::kSmem <= kTileSmemMax && TileCfg<2>::kSmem <= kTileSmemMax,
+static_assert(TileCfg<4, 1>::kSmem <= kTileSmemMax && TileCfg<4, 2>::kSmem <= kTileSmemMax,
               "decode kernel exceeds shared memory");
 
 template <int NW>
@@ -95,16 +102,18 @@ struct TileCtl {
     int w_lo[NW], w_hi[NW], w_first[NW];    // each warp's tile range and first slab
     int abort;
 };
-static_assert(sizeof(TileCtl<TileCfg<1>::kWarps>) <= TileCfg<1>::kCtlBytes &&
-                  sizeof(TileCtl<8>) <= TileCfg<2>::kCtlBytes &&
-                  TileCfg<1>::kStages <= kMaxTStages && TileCfg<2>::kStages <= kMaxTStages,
+static_assert(sizeof(TileCtl<TileCfg<4, 1>::kWarps>) <= TileCfg<4, 1>::kCtlBytes &&
+                  sizeof(TileCtl<8>) <= TileCfg<4, 2>::kCtlBytes &&
+                  TileCfg<4, 1>::kStages <= kMaxTStages && TileCfg<4, 2>::kStages <= kMaxTStages,
               "control block does not fit its shared-memory slot");
 
-template <int NB, int NW, bool XS>
+template <int BITS, int NB, int NW, bool XS>
 __global__ void __launch_bounds__(NW * 32, AWQ_TILE_MINBLOCKS) gemv_tiles_kernel(const TileParams p) {
-    using Cfg = TileCfg<NB>;
+    using Cfg = TileCfg<BITS, NB>;
     static_assert(Cfg::kWarps == NW, "warp count");
     constexpr int kStages = Cfg::kStages;
+    constexpr int kTStageBytes = Cfg::kStageBytes;
+    constexpr int kTB = Cfg::kTile;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
@@ -127,7 +136,7 @@ __global__ void __launch_bounds__(NW * 32, AWQ_TILE_MINBLOCKS) gemv_tiles_kernel
     const int n_st = (n_my + kTilesPerStage - 1) / kTilesPerStage;
     const int first_sl = u_lo / G;                      // this warp's first CTA-local slab
     uint8_t* my_ring = ring + (size_t)warp * kStages * kTStageBytes;
-    const uint8_t* cta_tiles = p.tiles + (int64_t)s0 * G * kTileBytes;
+    const uint8_t* cta_tiles = p.tiles + (int64_t)s0 * G * kTB;
 
     // Programmatic dependent launch (see the plain decode kernel): the next
     // kernel in the stream may start at once; X and inv_s are read and Y is
@@ -143,14 +152,15 @@ __global__ void __launch_bounds__(NW * 32, AWQ_TILE_MINBLOCKS) gemv_tiles_kernel
     auto issue = [&](int i, int s) {
         const int u = u_lo + i * kTilesPerStage;
         const int nt = min(kTilesPerStage, u_hi - u);
-        const uint32_t bytes = (uint32_t)(nt * kTileBytes);
+        const uint32_t bytes = (uint32_t)(nt * kTB);
         uint64_t* bar = &ctl->full[warp][s];
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_load(my_ring + (size_t)s * kTStageBytes, cta_tiles + (int64_t)u * kTileBytes, bytes,
-                  bar, pol);
+        bulk_load(my_ring + (size_t)s * kTStageBytes, cta_tiles + (int64_t)u * kTB, bytes, bar,
+                  pol);
     };
     if (warp == 0 && lane < p.M)
         bulk_prefetch_l2(p.X + (int64_t)lane * p.ldx, (uint32_t)(G * kGroup * 2));
+    // (3 bits: no fused input scaling, inv_s is null)
     if (warp == 0 && lane == 31 && p.inv_s)
         bulk_prefetch_l2(p.inv_s, (uint32_t)(G * kGroup * 4));
     const int n_first = min(kStages, n_st);
@@ -173,9 +183,13 @@ __global__ void __launch_bounds__(NW * 32, AWQ_TILE_MINBLOCKS) gemv_tiles_kernel
     const uint8_t* xs[NB];
     uint8_t* bs = nullptr;
     if constexpr (XS) {
-        const int64_t xrow = dec_x_row_bytes(G);
-        bs = xsm + (int64_t)p.M * xrow;
-        stage_x_folded<NB>(xsm, bs, p.X, p.ldx, p.M, p.inv_s, G, threadIdx.x, Cfg::kThreads);
+        const int64_t xrow = BITS == 4 ? dec_x_row_bytes(G) : dec_x3_row_bytes((int64_t)G * kGroup);
+        if constexpr (BITS == 4) {
+            bs = xsm + (int64_t)p.M * xrow;
+            stage_x_folded<NB>(xsm, bs, p.X, p.ldx, p.M, p.inv_s, G, threadIdx.x, Cfg::kThreads);
+        } else {
+            stage_x3(xsm, p.X, p.ldx, p.M, (int64_t)G * kGroup, threadIdx.x, Cfg::kThreads);
+        }
         __syncthreads();
         // lanes of absent tokens read the last token's row; their outputs
         // are dropped
@@ -245,18 +259,32 @@ __global__ void __launch_bounds__(NW * 32, AWQ_TILE_MINBLOCKS) gemv_tiles_kernel
                         for (int j = 0; j < 4; ++j) y[nb][j] = 0.0f;
                     cur = sl;
                 }
-                const uint8_t* tile = stage + jt * kTileBytes;
-                const uint4 wa = *reinterpret_cast<const uint4*>(tile + lane * 16);
-                const uint4 wb = *reinterpret_cast<const uint4*>(tile + 512 + lane * 16);
-                const uint2 sz = *reinterpret_cast<const uint2*>(tile + 1024 + g * 8);
-                if constexpr (XS) {
-                    group_mma_folded<NB>(y, sz, wa, wb, xs, bs, gi, t);
+                const uint8_t* tile = stage + jt * kTB;
+                if constexpr (BITS == 4) {
+                    const uint4 wa = *reinterpret_cast<const uint4*>(tile + lane * 16);
+                    const uint4 wb = *reinterpret_cast<const uint4*>(tile + 512 + lane * 16);
+                    const uint2 sz = *reinterpret_cast<const uint2*>(tile + 1024 + g * 8);
+                    if constexpr (XS) {
+                        group_mma_folded<NB>(y, sz, wa, wb, xs, bs, gi, t);
+                    } else {
+                        GroupX<NB> gx;
+                        load_group_x<NB>(gx, p.X, p.ldx, p.M, p.inv_s, gi, g, t);
+                        group_mma<NB, false>(y, (uint16_t)(sz.x & 0xFFFFu),
+                                             (uint16_t)(sz.y & 0xFFFFu), (uint16_t)(sz.x >> 16),
+                                             (uint16_t)(sz.y >> 16), gx, wa, wb, xs, gi, t);
+                    }
                 } else {
-                    GroupX<NB> gx;
-                    load_group_x<NB>(gx, p.X, p.ldx, p.M, p.inv_s, gi, g, t);
-                    group_mma<NB, false>(y, (uint16_t)(sz.x & 0xFFFFu), (uint16_t)(sz.y & 0xFFFFu),
-                                         (uint16_t)(sz.x >> 16), (uint16_t)(sz.y >> 16), gx, wa,
-                                         wb, xs, gi, t);
+                    // rows g and g + 8: 48 bytes of planes each, then the scales
+                    const uint4* ra = reinterpret_cast<const uint4*>(tile + 48 * g);
+                    const uint4* rb = reinterpret_cast<const uint4*>(tile + 48 * (g + 8));
+                    const uint4 a0 = ra[0], a1 = ra[1], a2 = ra[2];
+                    const uint4 b0 = rb[0], b1 = rb[1], b2 = rb[2];
+                    const uint32_t A[12] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y,
+                                            a1.z, a1.w, a2.x, a2.y, a2.z, a2.w};
+                    const uint32_t B[12] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y,
+                                            b1.z, b1.w, b2.x, b2.y, b2.z, b2.w};
+                    const uint2 sz = *reinterpret_cast<const uint2*>(tile + 768 + g * 8);
+                    group_mma3<NB, XS>(y, sz, A, B, xs, p.X, p.ldx, p.M, gi, g, t);
                 }
                 if (++gi == G) {
                     gi = 0;
@@ -305,13 +333,13 @@ __global__ void __launch_bounds__(NW * 32, AWQ_TILE_MINBLOCKS) gemv_tiles_kernel
     }
 }
 
-template <int NB, int NW, bool XS>
+template <int BITS, int NB, int NW, bool XS>
 cudaError_t launch_tiles_nb(const TileParams& p, int grid, size_t smem, cudaStream_t st) {
-    cudaError_t e = smem_attr_once<gemv_tiles_kernel<NB, NW, XS>>((int)kTileSmemMax);
+    cudaError_t e = smem_attr_once<gemv_tiles_kernel<BITS, NB, NW, XS>>((int)kTileSmemMax);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(TileCfg<NB>::kThreads);
+    cfg.blockDim = dim3(TileCfg<BITS, NB>::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -319,16 +347,18 @@ cudaError_t launch_tiles_nb(const TileParams& p, int grid, size_t smem, cudaStre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_tiles_kernel<NB, NW, XS>, p);
+    return cudaLaunchKernelEx(&cfg, gemv_tiles_kernel<BITS, NB, NW, XS>, p);
 }
 
-template <int NB, int NW>
+template <int BITS, int NB, int NW>
 cudaError_t launch_tiles_cfg(const TileParams& p, int grid, cudaStream_t st) {
+    using Cfg = TileCfg<BITS, NB>;
     const size_t xs_bytes =
-        (size_t)p.M * (size_t)dec_x_row_bytes(p.G) + (size_t)dec_bs_bytes(p.G, NB);
-    if (TileCfg<NB>::kSmem + xs_bytes <= kTileSmemMax)
-        return launch_tiles_nb<NB, NW, true>(p, grid, TileCfg<NB>::kSmem + xs_bytes, st);
-    return launch_tiles_nb<NB, NW, false>(p, grid, TileCfg<NB>::kSmem, st);
+        BITS == 4 ? (size_t)p.M * (size_t)dec_x_row_bytes(p.G) + (size_t)dec_bs_bytes(p.G, NB)
+                  : (size_t)p.M * (size_t)dec_x3_row_bytes((int64_t)p.G * kGroup);
+    if (Cfg::kSmem + xs_bytes <= kTileSmemMax)
+        return launch_tiles_nb<BITS, NB, NW, true>(p, grid, Cfg::kSmem + xs_bytes, st);
+    return launch_tiles_nb<BITS, NB, NW, false>(p, grid, Cfg::kSmem, st);
 }
 
 // One thread per 16 bytes of the tiled buffer (68 per tile): consecutive
@@ -369,7 +399,56 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// The 3-bit tiles: one thread per 16 bytes (52 per tile): 48 chunks of the
+// 16 rows' planes (row r's 48 bytes at 48 r), then the four of scales and
+// zero-points.
+__global__ void __launch_bounds__(256)
+    repack_int3_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restrict__ scales,
+                       const uint16_t* __restrict__ zeros, int64_t N, int64_t K,
+                       uint4* __restrict__ tiles, int64_t n_chunks) {
+    constexpr int kChunks = kTile3Bytes / 16;           // 52
+    const int64_t G = K / kGroup, wrow = K / 32 * 3;
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < n_chunks;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tile = u / kChunks;
+        const int c = (int)(u - tile * kChunks);
+        const int64_t j = tile / G, gi = tile - j * G;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (c < 48) {
+            const int64_t row = j * kDecRows + c / 3;
+            if (row < N)
+                v = __ldg(reinterpret_cast<const uint4*>(planes + row * wrow + gi * 12 + (c % 3) * 4));
+        } else {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int64_t ra = j * kDecRows + (c - 48) * 2 + e, rb = ra + 8;
+                const uint32_t sa = ra < N ? scales[ra * G + gi] : 0u;
+                const uint32_t za = ra < N ? zeros[ra * G + gi] : 0u;
+                const uint32_t sb = rb < N ? scales[rb * G + gi] : 0u;
+                const uint32_t zb = rb < N ? zeros[rb * G + gi] : 0u;
+                w[2 * e] = sa | (za << 16);
+                w[2 * e + 1] = sb | (zb << 16);
+            }
+            v = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        tiles[u] = v;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_repack_int3(const uint32_t* planes, const uint16_t* scales,
+                               const uint16_t* zeros, int64_t N, int64_t K, void* tiles,
+                               int num_sms, cudaStream_t st) {
+    const int64_t n_chunks = (N + kDecRows - 1) / kDecRows * (K / kGroup) * (kTile3Bytes / 16);
+    if (n_chunks == 0) return cudaSuccess;
+    int64_t blocks = (n_chunks + 255) / 256;
+    if (blocks > (int64_t)num_sms * 16) blocks = (int64_t)num_sms * 16;
+    repack_int3_kernel<<<(unsigned)blocks, 256, 0, st>>>(planes, scales, zeros, N, K,
+                                                         static_cast<uint4*>(tiles), n_chunks);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gemv_tiles(const TileParams& p, int num_sms, cudaStream_t st) {
     if (p.M <= 0 || p.N <= 0) return cudaSuccess;
@@ -377,8 +456,11 @@ cudaError_t launch_gemv_tiles(const TileParams& p, int num_sms, cudaStream_t st)
     const int grid = (int)(n_slabs < num_sms ? n_slabs : num_sms);
     // the kernel indexes a CTA's tiles in 32 bits
     if ((n_slabs / grid + 1) * (int64_t)p.G >= (1LL << 31)) return cudaErrorInvalidValue;
-    return p.M <= 8 ? launch_tiles_cfg<1, TileCfg<1>::kWarps>(p, grid, st)
-                    : launch_tiles_cfg<2, 8>(p, grid, st);
+    if (p.bits == 3)
+        return p.M <= 8 ? launch_tiles_cfg<3, 1, TileCfg<3, 1>::kWarps>(p, grid, st)
+                        : launch_tiles_cfg<3, 2, 8>(p, grid, st);
+    return p.M <= 8 ? launch_tiles_cfg<4, 1, TileCfg<4, 1>::kWarps>(p, grid, st)
+                    : launch_tiles_cfg<4, 2, 8>(p, grid, st);
 }
 
 cudaError_t launch_repack_int4(const uint32_t* qweight, const uint16_t* scales,

@@ -60,7 +60,8 @@ cudaError_t launch_gemv(const CUtensorMap& mapW, const GemvParams& p, int num_sm
 
 // ---- decode matmul over the repacked decode tiles, and the repack
 // (gemv_tiles.cu) ----
-constexpr int kTileBytes = 1088;   // one (16-row slab, group of 128) tile
+constexpr int kTileBytes = 1088;   // one (16-row slab, group of 128) tile, 4 bits
+constexpr int kTile3Bytes = 832;   // the same at 3 bits: 16 x 48 bytes of planes + 64
 struct TileParams {
     const uint16_t* X;
     int64_t ldx;
@@ -72,9 +73,13 @@ struct TileParams {
     int64_t ldy;
     unsigned* status;
     int early_weights;   // 1: weights may be fetched before the previous kernel completes
-    const float* inv_s;  // [K] or null: X is used as fp16(X * inv_s)
+    const float* inv_s;  // [K] or null: X is used as fp16(X * inv_s) (4 bits only)
+    int bits;            // 4 or 3 (tiles of kTileBytes or kTile3Bytes)
 };
 cudaError_t launch_gemv_tiles(const TileParams& p, int num_sms, cudaStream_t st);
+cudaError_t launch_repack_int3(const uint32_t* planes, const uint16_t* scales,
+                               const uint16_t* zeros, int64_t N, int64_t K, void* tiles,
+                               int num_sms, cudaStream_t st);
 cudaError_t launch_repack_int4(const uint32_t* qweight, const uint16_t* scales,
                                const uint16_t* zeros, int64_t N, int64_t K, void* tiles,
                                int num_sms, cudaStream_t st);
