@@ -117,10 +117,10 @@ __device__ __forceinline__ float rint_quot(float a, float b, float rb) {
     return rt;
 }
 
-// rint_quot for 8 values of one warp-uniform divisor, without a branch per
-// value: the fast roundings first, then -- only if some lane of the warp
-// met a near-tie -- the exact quotient for those values.  All 32 lanes of
-// the warp must call it together.
+// rint_quot for 8 values of one divisor (per lane; lanes may differ),
+// without a branch per value: the fast roundings first, then -- only if some
+// lane of the warp met a near-tie -- the exact quotient for those values.
+// All 32 lanes of the warp must call it together (the vote).
 __device__ __forceinline__ void rint_quot8(const float* a, float b, float rb, float* r) {
     bool tie = false;
 #pragma unroll

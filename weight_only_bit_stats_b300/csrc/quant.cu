@@ -13,6 +13,20 @@ namespace awq {
 namespace {
 
 constexpr int kCandThreads = 256;
+// Pack launch shape: 128-thread blocks held to 96 registers (five resident
+// per SM), grid capped at two waves of them.
+#ifndef AWQ_PACK_BLOCKS_PER_SM
+#define AWQ_PACK_BLOCKS_PER_SM 10
+#endif
+#ifndef AWQ_PACK_THREADS
+#define AWQ_PACK_THREADS 128
+#endif
+#ifndef AWQ_PACK_MIN_BLOCKS
+#define AWQ_PACK_MIN_BLOCKS 5
+#endif
+constexpr int kPackBlocksPerSm = AWQ_PACK_BLOCKS_PER_SM;
+constexpr int kPackThreads = AWQ_PACK_THREADS;
+constexpr int kPackMinBlocks = AWQ_PACK_MIN_BLOCKS;
 
 // Pass 1: r_k = pow(max(m_k, 1e-4), alpha) and per-block max / min of r.
 __global__ void __launch_bounds__(kCandThreads)
@@ -73,184 +87,224 @@ __global__ void __launch_bounds__(kCandThreads)
     }
 }
 
-// Eight lanes per (row, group), four row-groups per warp: lane c holds the
-// 16 channels 16c..16c+15 of its row-group, forms the group's range with
-// three shuffle rounds, rounds its 16 levels with the branch-free exact
-// quotient (the same levels as the search producer's), and writes its two
-// packed words; the eight lanes of a row-group write its 64 bytes at once.
-__global__ void __launch_bounds__(256)
-    pack_int4_kernel(const uint16_t* __restrict__ W, int64_t N, int64_t K, int64_t ldw,
-                     const float* __restrict__ s, uint32_t* __restrict__ qweight,
-                     uint16_t* __restrict__ scales, uint16_t* __restrict__ zeros,
-                     unsigned* status) {
-    const int lane = threadIdx.x & 31, c = lane & 7, rg = lane >> 3;
-    const int64_t G = K / kGroup;
-    const int64_t total = N * G;
-    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    bool bad = false;
-    // every lane runs the same number of iterations (the shuffles and the
-    // vote need the whole warp); lanes past the end work on a clamped item
-    for (int64_t base = warp0 * 4; base < total; base += nwarps * 4) {
-        const int64_t item = base + rg;
-        const bool live = item < total;
-        const int64_t it = live ? item : total - 1;
-        const int64_t n = it / G, g = it - n * G;
-        const int64_t k0 = g * kGroup + 16 * c;
-        const uint4* wp4 = reinterpret_cast<const uint4*>(W + n * ldw + k0);
-        const uint4 r0 = __ldg(wp4), r1 = __ldg(wp4 + 1);
-        float4 sv[4];
-        if (s) {
-            const float4* sp = reinterpret_cast<const float4*>(s + k0);
+// Level bits without a float-to-integer conversion: for an integer-valued
+// rt (or +-Inf, NaN, or any magnitude), fp32 min(max(rt + (z + 2^23), 2^23),
+// qmax + 2^23) is 2^23 + clamp(rt + z, 0, qmax) exactly (the sums are exact
+// below 2^24 in magnitude and rounding is monotone above), and its bit
+// pattern is 0x4B000000 + level.  Summing (0x4B000000 + L_e) 16^e over eight
+// levels modulo 2^32 leaves sum L_e 16^e plus 0x4B000000 + 0xB0000000 (the
+// higher terms of the constant vanish).
+__device__ __forceinline__ uint32_t nibbles8_exact(const float* wp, float scale, float rcp,
+                                                   float zf, float qmax) {
+    const float zb = __fadd_rn(zf, 8388608.0f), topb = qmax + 8388608.0f;
+    uint32_t acc = 0;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) sv[j] = __ldg(sp + j);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) sv[j] = make_float4(1.f, 1.f, 1.f, 1.f);
-        }
-        const uint32_t wr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-        const float* sf = reinterpret_cast<const float*>(sv);
-        float wp[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const uint32_t h = (wr[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-            wp[e] = __fmul_rn(__half2float(__ushort_as_half((unsigned short)h)), sf[e]);
-        }
-        float lo = wp[0], hi = wp[0];
-#pragma unroll
-        for (int e = 1; e < 16; ++e) {
-            lo = fmin_nan(lo, wp[e]);
-            hi = fmax_nan(hi, wp[e]);
-        }
-        // this lane's 16 values: NaN or Inf makes lo or hi non-finite
-        const bool lane_bad = !(isfinite(lo) && isfinite(hi));
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
-            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-            hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-        }
-        const GroupQuant gq = group_quant_from_range(lo, hi);
-        if (live) bad |= lane_bad || !gq.finite;
-        float rt[16];
-        rint_quot8(wp, gq.scale, gq.rcp, rt);
-        rint_quot8(wp + 8, gq.scale, gq.rcp, rt + 8);
-        uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            w0 |= (uint32_t)fminf(fmaxf(__fadd_rn(rt[e], gq.zf), 0.0f), 15.0f) << (4 * e);
-            w1 |= (uint32_t)fminf(fmaxf(__fadd_rn(rt[e + 8], gq.zf), 0.0f), 15.0f) << (4 * e);
-        }
-        if (live) {
-            *reinterpret_cast<uint2*>(qweight + n * (K / 8) + g * 16 + 2 * c) = make_uint2(w0, w1);
-            if (c == 0) {
-                scales[n * G + g] = __half_as_ushort(gq.scale_h);
-                zeros[n * G + g] = __half_as_ushort(__float2half_rn(gq.zf));
-            }
-        }
+    for (int e = 0; e < 8; ++e) {
+        const float t0 = __fmul_rn(wp[e], rcp);
+        float rt = rint_small(t0);
+        if (near_tie(t0, rt)) rt = rintf(__fdiv_rn(wp[e], scale));
+        acc += __float_as_uint(fminf(fmaxf(__fadd_rn(rt, zb), 8388608.0f), topb)) << (4 * e);
     }
-    if (bad) set_status(status, kStatusNonFinite);
+    return acc - 0xFB000000u;
 }
 
-// Group parameters at 3 bits: the rule of group_quant_from_range with the
-// top level 7 instead of 15 (d = fp32(range / 7), zero-point clamped to 0..7).
-// The exact-quotient rounding holds unchanged: only quotients below 8 in
-// magnitude can leave the clamp.
-__device__ __forceinline__ GroupQuant group_quant3_from_range(float lo, float hi) {
-    GroupQuant g;
-    const float range = __fsub_rn(hi, lo);
-    float d = __fdiv_rn(range, 7.0f);
-    d = fmaxf(d, 6.103515625e-05f);              // 2^-14, least normal fp16
-    g.scale_h = __float2half_rn(d);
-    g.scale = __half2float(g.scale_h);
-    g.finite = isfinite(g.scale);
-    g.rcp = __frcp_rn(g.scale);
-    const float z = rint_quot(-lo, g.scale, g.rcp);
-    g.zf = z > 0.0f ? fminf(z, 7.0f) : 0.0f;
-    return g;
+// Bit p of each of the 8 nibbles of w, as 8 contiguous bits.
+__device__ __forceinline__ uint32_t nibble_plane(uint32_t w, int p) {
+    uint32_t x = (w >> p) & 0x11111111u;
+    x = (x | (x >> 3)) & 0x03030303u;
+    x = (x | (x >> 6)) & 0x000F000Fu;
+    return (x | (x >> 12)) & 0xFFu;
 }
 
-// 3-bit pack ("3 and 4 bits", AWQ page, fourth paragraph): the layout of
-// pack_int4_kernel's lanes (8 per row-group, 16 channels each), levels
-// 0..7, and three bit planes per 32 levels.  A lane sets bit p of its 16
-// levels in the low or high half of plane word p; the lane pair of a 32-level
-// block ORs its halves and the even lane writes the block's three words.
-__global__ void __launch_bounds__(256)
-    pack_int3_kernel(const uint16_t* __restrict__ W, int64_t N, int64_t K, int64_t ldw,
-                     const float* __restrict__ s, uint32_t* __restrict__ planes,
-                     uint16_t* __restrict__ scales, uint16_t* __restrict__ zeros,
-                     unsigned* status) {
-    const int lane = threadIdx.x & 31, c = lane & 7, rg = lane >> 3;
+// The fast levels of 32 scaled weights (16 pairs) as four nibble words
+// (eight levels each), and whether any quotient came near a tie.  y =
+// fp32(t + 1.5 * 2^23) holds rint(t) in its low mantissa bits for |t| <
+// 2^22: with t clamped to [-z, qmax - z] (CLAMP), or known to round inside
+// it, the bit pattern of y is 0x4B400000 + rint(t), so the level rint(t) + z
+// is the pattern minus 0x4B400000 - z.  Clamping t before rounding equals
+// clamping after, the bounds being integers; a clamped t is an integer and
+// is never near a tie.  The pair operations round each lane as the scalar
+// ones do.
+template <bool CLAMP>
+__device__ __forceinline__ bool fast_nibbles32(const float2* wp, float rcp, float zf, float qmax,
+                                               uint32_t* w) {
+    const float kM = 12582912.0f;               // 1.5 * 2^23
+    const float2 rcp2 = make_float2(rcp, rcp), m2 = make_float2(kM, kM);
+    const float2 negm2 = make_float2(-kM, -kM), neg1 = make_float2(-1.0f, -1.0f);
+    const float lo = -zf, hi = qmax - zf;
+    const uint32_t bias = (0x4B400000u - (uint32_t)zf) * 0x11111111u;
+    float dmax[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t acc = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float2 t = __fmul2_rn(wp[4 * i + e], rcp2);
+            if (CLAMP) {
+                t.x = fminf(fmaxf(t.x, lo), hi);
+                t.y = fminf(fmaxf(t.y, lo), hi);
+            }
+            const float2 y = __fadd2_rn(t, m2);
+            const float2 d = __ffma2_rn(__fadd2_rn(y, negm2), neg1, t);   // t - rint(t)
+            dmax[e] = fmaxf(dmax[e], fmaxf(fabsf(d.x), fabsf(d.y)));
+            acc += __float_as_uint(y.x) << (8 * e);
+            acc += __float_as_uint(y.y) << (8 * e + 4);
+        }
+        w[i] = acc - bias;
+    }
+    return fmaxf(fmaxf(dmax[0], dmax[1]), fmaxf(dmax[2], dmax[3])) > kTieBand;
+}
+
+// Four lanes per (row, group), eight row-groups per warp.  A row-group is
+// 16 chunks of 8 channels (16 bytes of W each); lane c holds chunks 4j + c,
+// j = 0..3, so each of its four 16-byte loads reads 64 contiguous bytes of
+// the row across the four lanes.  A warp's unit is eight consecutive rows of
+// one group g: the warp stages s for g in its own shared-memory slice (one
+// 512-byte load), which the eight row-groups then read as broadcasts.  Units
+// are walked with a fixed stride kept as a quotient and remainder of G, so
+// that no iteration divides.
+//
+// The group's range takes two shuffle rounds; the 32 levels of a lane use
+// the branch-free exact quotient (the same levels as the search producer's).
+// When rint(lo / d) and rint(hi / d) (the fast quotients of the group's
+// extremes; every quotient of the group lies between them) already fall in
+// [-z, qmax - z] for every row-group of the warp, no level can leave 0..qmax
+// and the clamp is skipped.  When any quotient of the warp comes near a tie,
+// the warp recomputes its levels with the exact quotient.
+//
+// BITS = 4: chunk 4j + c is packed word 4j + c of the row-group.  BITS = 3
+// ("3 and 4 bits", AWQ page, fourth paragraph): levels 0..7 in three bit
+// planes per 32-level block; block j is chunks 4j..4j+3, one per lane, so
+// the lanes' plane bytes are transposed across the four lanes (two shuffle
+// rounds with byte permutes) and lane c writes block c's three words.
+template <int BITS>
+__global__ void __launch_bounds__(kPackThreads, kPackMinBlocks)
+    pack_kernel(const uint16_t* __restrict__ W, int64_t N, int64_t K, int64_t ldw,
+                const float* __restrict__ s, uint32_t* __restrict__ out,
+                uint16_t* __restrict__ scales, uint16_t* __restrict__ zeros, unsigned* status) {
+    constexpr float kQmax = (float)((1 << BITS) - 1);
+    __shared__ __align__(16) float s_sh[kPackThreads / 32][kGroup];
+    const int lane = threadIdx.x & 31, c = lane & 3, rg = lane >> 2;
+    float* ss = s_sh[threadIdx.x >> 5];
     const int64_t G = K / kGroup;
-    const int64_t total = N * G;
-    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t chunks = (N + 7) / 8, units = chunks * G;
+    const int64_t unit0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t sq = stride / G, sr = stride - sq * G;
+    int64_t chunk = unit0 / G, g = unit0 - chunk * G;
+    // byte-transpose selectors of the 3-bit planes (lane-dependent)
+    const uint32_t sel2 = (c & 2) ? 0x3276u : 0x5410u, sel1 = (c & 1) ? 0x3715u : 0x6240u;
+    // unit (chunk, g) -> this lane's four 16-byte pieces of W and the warp's
+    // 512-byte piece of s for g (rows past N - 1 read row N - 1)
+    auto fetch = [&](int64_t ch, int64_t gg, uint4* raw, float4& sv) {
+        const int64_t n = ch * 8 + rg;
+        const uint4* wp4 = reinterpret_cast<const uint4*>(W + (n < N ? n : N - 1) * ldw + gg * kGroup);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) raw[j] = __ldg(wp4 + 4 * j + c);
+        sv = s ? __ldg(reinterpret_cast<const float4*>(s + gg * kGroup) + lane)
+               : make_float4(1.f, 1.f, 1.f, 1.f);
+    };
     bool bad = false;
-    for (int64_t base = warp0 * 4; base < total; base += nwarps * 4) {
-        const int64_t item = base + rg;
-        const bool live = item < total;
-        const int64_t it = live ? item : total - 1;
-        const int64_t n = it / G, g = it - n * G;
-        const int64_t k0 = g * kGroup + 16 * c;
-        const uint4* wp4 = reinterpret_cast<const uint4*>(W + n * ldw + k0);
-        const uint4 r0 = __ldg(wp4), r1 = __ldg(wp4 + 1);
-        float4 sv[4];
-        if (s) {
-            const float4* sp = reinterpret_cast<const float4*>(s + k0);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) sv[j] = __ldg(sp + j);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) sv[j] = make_float4(1.f, 1.f, 1.f, 1.f);
+    uint4 raw[4];
+    float4 sv;
+    if (unit0 < units) fetch(chunk, g, raw, sv);
+    // every lane runs the same number of iterations (the shuffles and votes
+    // need the whole warp); lanes past the last row work on row N - 1 and
+    // write nothing.  The next unit's loads are issued before this unit's
+    // arithmetic.
+    for (int64_t u = unit0; u < units; u += stride) {
+        const int64_t n = chunk * 8 + rg;
+        const bool live = n < N;
+        const int64_t nn = live ? n : N - 1;
+        int64_t g_next = g + sr, chunk_next = chunk + sq;
+        if (g_next >= G) {
+            g_next -= G;
+            ++chunk_next;
         }
-        const uint32_t wr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-        const float* sf = reinterpret_cast<const float*>(sv);
-        float wp[16];
+        uint4 raw_next[4];
+        float4 sv_next;
+        if (u + stride < units) fetch(chunk_next, g_next, raw_next, sv_next);   // warp-uniform
+        __syncwarp();                       // the previous unit's reads of ss are done
+        reinterpret_cast<float4*>(ss)[lane] = sv;
+        __syncwarp();
+        float2 wp2[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const uint32_t h = (wr[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-            wp[e] = __fmul_rn(__half2float(__ushort_as_half((unsigned short)h)), sf[e]);
-        }
-        float lo = wp[0], hi = wp[0];
+        for (int j = 0; j < 4; ++j) {
+            const float4 sa = reinterpret_cast<const float4*>(ss)[8 * j + 2 * c];
+            const float4 sb = reinterpret_cast<const float4*>(ss)[8 * j + 2 * c + 1];
+            const float2 sf[4] = {make_float2(sa.x, sa.y), make_float2(sa.z, sa.w),
+                                  make_float2(sb.x, sb.y), make_float2(sb.z, sb.w)};
+            const uint32_t rw[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
 #pragma unroll
-        for (int e = 1; e < 16; ++e) {
-            lo = fmin_nan(lo, wp[e]);
-            hi = fmax_nan(hi, wp[e]);
+            for (int h = 0; h < 4; ++h)
+                wp2[4 * j + h] =
+                    __fmul2_rn(__half22float2(*reinterpret_cast<const __half2*>(&rw[h])), sf[h]);
         }
+        // four independent min / max chains, then their combination
+        float lq[4], hq[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            lq[q] = fmin_nan(wp2[q].x, wp2[q].y);
+            hq[q] = fmax_nan(wp2[q].x, wp2[q].y);
+        }
+#pragma unroll
+        for (int e = 4; e < 16; ++e) {
+            lq[e & 3] = fmin3_nan(lq[e & 3], wp2[e].x, wp2[e].y);
+            hq[e & 3] = fmax3_nan(hq[e & 3], wp2[e].x, wp2[e].y);
+        }
+        float lo = fmin_nan(fmin3_nan(lq[0], lq[1], lq[2]), lq[3]);
+        float hi = fmax_nan(fmax3_nan(hq[0], hq[1], hq[2]), hq[3]);
+        const float* wp = reinterpret_cast<const float*>(wp2);
+        // this lane's 32 values: NaN or Inf makes lo or hi non-finite
         const bool lane_bad = !(isfinite(lo) && isfinite(hi));
 #pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
+        for (int o = 1; o < 4; o <<= 1) {
             lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
             hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
         }
-        const GroupQuant gq = group_quant3_from_range(lo, hi);
+        const GroupQuant gq = group_quant_from_range(lo, hi, kQmax);
         if (live) bad |= lane_bad || !gq.finite;
-        float rt[16];
-        rint_quot8(wp, gq.scale, gq.rcp, rt);
-        rint_quot8(wp + 8, gq.scale, gq.rcp, rt + 8);
-        uint32_t p0 = 0, p1 = 0, p2 = 0;
-        const int sh = 16 * (c & 1);
+        const bool inside = rint_small(__fmul_rn(lo, gq.rcp)) >= -gq.zf &&
+                            rint_small(__fmul_rn(hi, gq.rcp)) <= kQmax - gq.zf;
+        uint32_t w[4];
+        const bool tie = __all_sync(0xffffffffu, inside)
+                             ? fast_nibbles32<false>(wp2, gq.rcp, gq.zf, kQmax, w)
+                             : fast_nibbles32<true>(wp2, gq.rcp, gq.zf, kQmax, w);
+        if (__any_sync(0xffffffffu, tie)) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const uint32_t q = (uint32_t)fminf(fmaxf(__fadd_rn(rt[e], gq.zf), 0.0f), 7.0f);
-            p0 |= (q & 1u) << (sh + e);
-            p1 |= ((q >> 1) & 1u) << (sh + e);
-            p2 |= (q >> 2) << (sh + e);
+            for (int i = 0; i < 4; ++i)
+                w[i] = nibbles8_exact(wp + 8 * i, gq.scale, gq.rcp, gq.zf, kQmax);
         }
-        p0 |= __shfl_xor_sync(0xffffffffu, p0, 1);
-        p1 |= __shfl_xor_sync(0xffffffffu, p1, 1);
-        p2 |= __shfl_xor_sync(0xffffffffu, p2, 1);
-        if (live) {
-            if ((c & 1) == 0) {
-                uint32_t* w = planes + n * (K / 32 * 3) + g * 12 + (c >> 1) * 3;
-                w[0] = p0;
-                w[1] = p1;
-                w[2] = p2;
+        if constexpr (BITS == 4) {
+            if (live) {
+                uint32_t* pw = out + nn * (K / 8) + g * 16 + c;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) pw[4 * j] = w[j];
             }
-            if (c == 0) {
-                scales[n * G + g] = __half_as_ushort(gq.scale_h);
-                zeros[n * G + g] = __half_as_ushort(__float2half_rn(gq.zf));
+        } else {
+            uint32_t pl[3];
+#pragma unroll
+            for (int p = 0; p < 3; ++p) {
+                uint32_t v = nibble_plane(w[0], p) | (nibble_plane(w[1], p) << 8) |
+                             (nibble_plane(w[2], p) << 16) | (nibble_plane(w[3], p) << 24);
+                v = __byte_perm(v, __shfl_xor_sync(0xffffffffu, v, 2), sel2);
+                pl[p] = __byte_perm(v, __shfl_xor_sync(0xffffffffu, v, 1), sel1);
+            }
+            if (live) {
+                uint32_t* pw = out + nn * (K / 32 * 3) + g * 12 + 3 * c;
+#pragma unroll
+                for (int p = 0; p < 3; ++p) pw[p] = pl[p];
             }
         }
+        if (live && c == 0) {
+            scales[nn * G + g] = __half_as_ushort(gq.scale_h);
+            zeros[nn * G + g] = __half_as_ushort(__float2half_rn(gq.zf));
+        }
+        g = g_next;
+        chunk = chunk_next;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) raw[j] = raw_next[j];
+        sv = sv_next;
     }
     if (bad) set_status(status, kStatusNonFinite);
 }
@@ -316,6 +370,16 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// A warp per unit of eight rows of one group, at most kPackBlocksPerSm
+// blocks per SM.
+unsigned pack_blocks(int64_t N, int64_t K, int num_sms) {
+    const int64_t units = (N + 7) / 8 * (K / kGroup);
+    const int64_t warps = kPackThreads / 32;
+    const int64_t blocks = (units + warps - 1) / warps;
+    const int64_t cap = (int64_t)num_sms * kPackBlocksPerSm;
+    return (unsigned)(blocks < cap ? blocks : cap);
+}
+
 }  // namespace
 
 cudaError_t launch_scale_x(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
@@ -347,11 +411,8 @@ cudaError_t launch_pack_int4(const uint16_t* W, int64_t N, int64_t K, int64_t ld
                              int num_sms, cudaStream_t st) {
     const int64_t items = N * (K / kGroup);
     if (items == 0) return cudaSuccess;
-    int64_t blocks = (items + 31) / 32;               // 8 warps x 4 row-groups
-    const int64_t cap = (int64_t)num_sms * 8;
-    if (blocks > cap) blocks = cap;
-    pack_int4_kernel<<<(unsigned)blocks, 256, 0, st>>>(W, N, K, ldw, s, qweight, scales, zeros,
-                                                       status);
+    pack_kernel<4><<<pack_blocks(N, K, num_sms), kPackThreads, 0, st>>>(W, N, K, ldw, s, qweight, scales,
+                                                                 zeros, status);
     return cudaGetLastError();
 }
 
@@ -360,11 +421,8 @@ cudaError_t launch_pack_int3(const uint16_t* W, int64_t N, int64_t K, int64_t ld
                              int num_sms, cudaStream_t st) {
     const int64_t items = N * (K / kGroup);
     if (items == 0) return cudaSuccess;
-    int64_t blocks = (items + 31) / 32;               // 8 warps x 4 row-groups
-    const int64_t cap = (int64_t)num_sms * 8;
-    if (blocks > cap) blocks = cap;
-    pack_int3_kernel<<<(unsigned)blocks, 256, 0, st>>>(W, N, K, ldw, s, planes, scales, zeros,
-                                                       status);
+    pack_kernel<3><<<pack_blocks(N, K, num_sms), kPackThreads, 0, st>>>(W, N, K, ldw, s, planes, scales,
+                                                                 zeros, status);
     return cudaGetLastError();
 }
 
