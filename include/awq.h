@@ -286,7 +286,9 @@ size_t w4a16_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
  * exactly as w4a16_gemm uses X (so the result equals w4a16_gemm on those
  * fp16 values).  For M <= 16 the scaling happens as the decode kernel stages
  * its activations; for M > 16 a pre-pass writes the scaled activations into
- * the workspace.
+ * the workspace, and the tensor-core matmul, launched as its programmatic
+ * dependent, starts dequantising weights while the pre-pass runs (the
+ * pre-pass writes only the workspace).
  *   X      [M, K] fp16 unscaled, leading dimension ldx.
  *   inv_s  [K] fp32 device, 1/s per input channel (16-byte aligned).
  *   other arguments as w4a16_gemm; workspace >=
@@ -359,15 +361,18 @@ awq_status w3a16_gemm_repacked(const uint16_t* X, int64_t M, int64_t K, int64_t 
                                const void* tiles, int64_t N, int group, uint16_t* Y, int64_t ldy,
                                awq_stream_t stream);
 
-/* Overlap of back-to-back decode matmuls (M <= 16).  Every decode launch
- * lets the next kernel in the stream start beside it (programmatic dependent
- * launch) and reads X / writes Y only after the previous kernel in the stream
- * has completed.  With enable = 1 it also starts fetching its packed weights
- * (qweight, scales, zeros) before that point, so consecutive matmuls keep
- * HBM busy across kernel boundaries, as in a decode step where the weights
- * are constant.  Enable it only if no kernel that writes a matmul's packed
- * weights (awq_pack_int4 or any other) is the kernel immediately before that
- * w4a16_gemm call in its stream; otherwise the matmul may read stale weights.
+/* Overlap of back-to-back matmuls.  Every decode launch (M <= 16) lets the
+ * next kernel in the stream start beside it (programmatic dependent launch),
+ * and every matmul launch (decode and tensor-core) may start beside the
+ * previous kernel; each reads X / writes Y only after the previous kernel in
+ * the stream has completed.  With enable = 1 a matmul also starts fetching
+ * (decode) or dequantising (M > 16) its packed weights (qweight or planes,
+ * scales, zeros; the repacked tiles) before that point, so consecutive
+ * matmuls keep HBM busy across kernel boundaries, as in a decode step where
+ * the weights are constant.  Enable it only if no kernel that writes a
+ * matmul's packed weights (awq_pack_int4 or any other) is the kernel
+ * immediately before that matmul call in its stream; otherwise the matmul
+ * may read stale weights.
  * Process-wide setting, default 0.  Returns AWQ_ERR_INVALID_ARG unless
  * enable is 0 or 1.  (Host-side setting; the pages describe no counterpart
  * beyond memory-bound decoding with fused 4-bit kernels.) */

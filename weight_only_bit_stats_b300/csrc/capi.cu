@@ -652,6 +652,7 @@ awq_status w3a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
         p.Y = Y;
         p.ldy = ldy;
         p.status = d->status;
+        p.early_w = g_early_weights.load(std::memory_order_relaxed);
         e = awq::launch_tc_gemm3(map, p, d->num_sms, (cudaStream_t)stream);
     }
     return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
@@ -802,6 +803,9 @@ awq_status gemm_impl(const char* name, const uint16_t* X, int64_t M, int64_t K, 
         p.Y = Y;
         p.ldy = ldy;
         p.status = d->status;
+        // after the scaling pre-pass (which writes only Xs) the weights may
+        // be read early; otherwise only when the caller allows it
+        p.early_w = inv_s ? 1 : g_early_weights.load(std::memory_order_relaxed);
         if (k_splits > 1) p.ws_partial = reinterpret_cast<float*>(ws + xs_bytes);
         e = awq::launch_tc_gemm(map, p, d->num_sms, st);
         if (e == cudaSuccess && k_splits > 1)

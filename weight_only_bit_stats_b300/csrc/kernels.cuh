@@ -114,6 +114,10 @@ struct TcParams {
     float qmax;
     // 3-bit GEMM: bit planes [N][K/32][3] in place of qw
     const uint32_t* planes;
+    // GEMM modes: the weight producers may read qw / planes, scales and
+    // zeros before the previous kernel in the stream has completed (that
+    // kernel writes none of them)
+    int early_w;
 };
 constexpr int kTcRows = 128;          // weight rows per tile (UMMA M)
 constexpr int kTcTokens = 256;        // tokens per accumulator slot (UMMA N)

@@ -350,6 +350,7 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     scale_x_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K, int64_t ldx,
                    const float* __restrict__ inv_s, uint16_t* __restrict__ Xs) {
+    grid_dep_launch();          // the matmul's set-up and weight loads may start now
     const int64_t per_row = K / 8, total = M * per_row;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {

@@ -807,6 +807,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
+    // Launched as a programmatic dependent: the set-up above overlapped the
+    // previous kernel; every role waits for its writes here, except the
+    // weight producers of a GEMM whose previous kernel writes no weights.
+    if (!(is_gemm<MODE>() && p.early_w && warp >= kWarpProd0)) grid_dep_wait();
 
     if (warp == kWarpTma) {
         if (lane == 0) role_tma<MODE>(&mapX, &mapA, p, As, Bs, ctl);
@@ -843,8 +847,17 @@ cudaError_t launch_tc(const CUtensorMap& mapX, const CUtensorMap& mapA, const Tc
     cudaError_t e = smem_attr_once<tc_kernel<MODE>>((int)kSmem);
     if (e != cudaSuccess) return e;
     const int grid = p.n_items < num_sms ? p.n_items : num_sms;
-    tc_kernel<MODE><<<grid, Cfg<MODE>::kThreads, kSmem, st>>>(mapX, mapA, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(Cfg<MODE>::kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_kernel<MODE>, mapX, mapA, p);
 }
 
 __global__ void __launch_bounds__(256)
