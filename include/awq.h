@@ -265,9 +265,13 @@ awq_status w3a16_gemm(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
  *   qweight, scales, zeros: as written by awq_pack_int4 for an [N, K] weight.
  *   Y        [M, N] fp16, leading dimension ldy (>= N).
  * M <= 16 runs the decode kernel (packed weights streamed once, dequantised
- * in registers); M > 16 runs the tcgen05 tensor-core kernel, with K split
- * over several CTAs (fp32 partials in the workspace, added in order) when
- * the grid would otherwise be under-filled.
+ * in registers); M > 16 runs the tcgen05 tensor-core kernel, one 128-row x
+ * 256-token output tile per CTA in turn.  When the tiles would leave the
+ * grid under-filled, either every tile's K range is split over several CTAs
+ * or (stream-K tail) the whole waves of tiles run as they are and the K
+ * range of the remaining tiles is cut into one equal share per SM; in both
+ * cases the fp32 partials go to the workspace and are added in a fixed
+ * order (repeated calls give identical results).
  * workspace >= w4a16_gemm_workspace_size(M, N, K) bytes on the device that
  * runs the call (may be 0/NULL when that size is 0; 16-byte aligned).
  * K % 128 == 0, N % 8 == 0, group == 128. */

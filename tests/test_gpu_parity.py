@@ -320,6 +320,25 @@ def test_tensor_core_gemm_parity(wb, orc, M, N, K):
     _gemm_check(wb, orc, N, K, M)
 
 
+@pytest.mark.parametrize("M,N,K", [(300, 384, 16384), (513, 256, 16384), (257, 9856, 2048)])
+def test_gemm_stream_k_tail(wb, orc, M, N, K):
+    """Tile counts that leave a partial last wave on B300's 148 SMs (3 and 6
+    tiles with K = 16384; one whole wave of 148 tiles plus 6), for which the
+    K range of the last tiles is shared out over all CTAs and their fp32
+    partial tiles added afterwards: every output against the oracle, and
+    repeated calls bit-identical (the partials are added in a fixed order)."""
+    y = _gemm_check(wb, orc, N, K, M, seed=7)
+    W, _, X, _ = sg.layer_inputs(13, 7, N, K, 0, M=M)
+    rq, rs, rz = orc.pack_int4(W)
+    x, qw = dev(X), dev(rq.view(np.int32))
+    sc, ze = dev(rs.view(np.float16)), dev(rz.view(np.float16))
+    for _ in range(2):
+        Y = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+        wb.w4a16_gemm(x, qw, sc, ze, out=Y)
+        assert np.array_equal(host(Y).view(np.uint16), y.view(np.uint16))
+    wb.sync_status()
+
+
 def test_decode_rows_consistent(wb, orc):
     """Token 0 of a 16-token decode equals the 1-token decode exactly."""
     W, _, X, _ = sg.layer_inputs(14, 0, 1024, 2048, 0, M=16)

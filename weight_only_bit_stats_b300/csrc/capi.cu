@@ -6,6 +6,7 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include <atomic>
+#include <cmath>
 #include <mutex>
 
 #include "awq.h"
@@ -683,29 +684,58 @@ awq_status awq_pack_int3(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, c
 
 namespace {
 
-// K splits of the tensor-core GEMM: the count that minimises the modelled
-// time, waves x (groups per split) x (one group of one 128 x 256 tile,
-// about 1 us on B300) plus the split partials' extra traffic (written and
-// read once, fp32, at about 5 TB/s).  Splitting pays only for under-filled
-// grids with long K (e.g. 64 output tiles with K = 28672).
-int gemm_k_splits(int64_t M, int64_t N, int64_t K, int num_sms) {
-    if (M <= 16 || num_sms <= 0) return 1;
+// Work split of the tensor-core GEMM.  The modelled time is waves x
+// (groups per item) x (one group of one 128 x 256 tile, about 1 us on B300)
+// plus the partials' extra traffic (written and read once, fp32, at about
+// 5 TB/s).  Two ways to fill the grid beside plain whole tiles:
+//  - K splits: every tile's K range in k_splits equal parts (fp32 partials
+//    laid out like Y); pays for under-filled grids with long K;
+//  - stream-K tail: whole waves of tiles, then the K range of the remaining
+//    tiles (fewer than the SMs) cut into equal shares, one per SM (fp32
+//    partial tiles, two slots per SM), so the last wave is not mostly idle.
+// A split must win clearly (3%) over the plainer schedule.
+struct GemmSched {
+    int k_splits = 1;
+    int sk_full = 0, sk_tiles = 0;     // stream-K tail when sk_tiles > 0
+};
+
+GemmSched gemm_schedule(int64_t M, int64_t N, int64_t K, int num_sms) {
+    GemmSched sc;
+    if (M <= 16 || num_sms <= 0) return sc;
     const int64_t G = K / AWQ_GROUP;
     const int64_t tiles = ((N + awq::kTcRows - 1) / awq::kTcRows) *
                           ((M + awq::kGemmTokensPerItem - 1) / awq::kGemmTokensPerItem);
-    int best = 1;
     double best_t = 1e300;
     for (int ks = 1; ks <= 8; ++ks) {
         if (G / ks < 4) break;
         const int64_t waves = (tiles * ks + num_sms - 1) / num_sms;
         const double t = (double)waves * ((double)G / ks) * 1e-6 +
                          (ks > 1 ? 2.0 * ks * (double)M * (double)N * 4.0 / 5e12 : 0.0);
-        if (t < best_t * 0.97) {       // a split must win clearly
+        if (t < best_t * 0.97) {
             best_t = t;
-            best = ks;
+            sc.k_splits = ks;
         }
     }
-    return best;
+    const int64_t R = tiles % num_sms;
+    if (R > 0 && G >= 4 && num_sms <= 256) {      // (the fixup lists <= 512 slots a tile)
+        const double tile_bytes = (double)awq::kTcRows * awq::kTcTokens * 4.0;
+        const double t = (double)(tiles / num_sms) * (double)G * 1e-6 +
+                         std::ceil((double)(R * G) / num_sms) * 1e-6 +
+                         2.0 * (double)(num_sms + R) * tile_bytes / 5e12 + 3e-6;
+        if (t < best_t * 0.97) {
+            sc.k_splits = 1;
+            sc.sk_full = (int)(tiles - R);
+            sc.sk_tiles = (int)R;
+        }
+    }
+    return sc;
+}
+
+// Workspace bytes of a schedule (after the scaled-X pre-pass's share).
+size_t sched_ws_bytes(const GemmSched& sc, int64_t M, int64_t N, int num_sms) {
+    if (sc.sk_tiles > 0)
+        return (size_t)2 * (size_t)num_sms * awq::kTcRows * awq::kTcTokens * sizeof(float);
+    return sc.k_splits > 1 ? (size_t)sc.k_splits * (size_t)M * (size_t)N * sizeof(float) : 0;
 }
 
 int current_num_sms() {
@@ -721,8 +751,8 @@ extern "C" {
 
 size_t w4a16_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (M <= 16 || N <= 0 || K <= 0 || K % AWQ_GROUP) return 0;
-    const int ks = gemm_k_splits(M, N, K, current_num_sms());
-    return ks > 1 ? (size_t)ks * (size_t)M * (size_t)N * sizeof(float) : 0;
+    const int sms = current_num_sms();
+    return sched_ws_bytes(gemm_schedule(M, N, K, sms), M, N, sms);
 }
 
 }  // extern "C"
@@ -769,9 +799,9 @@ awq_status gemm_impl(const char* name, const uint16_t* X, int64_t M, int64_t K, 
     } else {
         uint8_t* ws = static_cast<uint8_t*>(workspace);
         const size_t xs_bytes = inv_s ? scaled_x_bytes(M, K) : 0;
-        const int k_splits = gemm_k_splits(M, N, K, d->num_sms);
-        const size_t part_bytes =
-            k_splits > 1 ? (size_t)k_splits * (size_t)M * (size_t)N * sizeof(float) : 0;
+        const GemmSched sc = gemm_schedule(M, N, K, d->num_sms);
+        const int k_splits = sc.k_splits;
+        const size_t part_bytes = sched_ws_bytes(sc, M, N, d->num_sms);
         if ((xs_bytes + part_bytes) > 0 &&
             (!workspace || ws_bytes < xs_bytes + part_bytes || !aligned16(workspace)))
             return fail(AWQ_ERR_WORKSPACE, "w4a16_gemm: workspace missing or too small "
@@ -797,6 +827,13 @@ awq_status gemm_impl(const char* name, const uint16_t* X, int64_t M, int64_t K, 
         p.t_tiles = (int)((M + awq::kGemmTokensPerItem - 1) / awq::kGemmTokensPerItem);
         p.k_splits = k_splits;
         p.n_items = p.n_tiles * p.t_tiles * k_splits;
+        if (sc.sk_tiles > 0) {
+            p.sk_full = sc.sk_full;
+            p.sk_tiles = sc.sk_tiles;
+            p.sk_ctas = d->num_sms;
+            p.n_items = sc.sk_full + d->num_sms;      // launches sk_ctas CTAs
+            p.ws_sk = reinterpret_cast<float*>(ws + xs_bytes);
+        }
         p.qw = qweight;
         p.scales = scales;
         p.zeros = zeros;
@@ -810,6 +847,7 @@ awq_status gemm_impl(const char* name, const uint16_t* X, int64_t M, int64_t K, 
         e = awq::launch_tc_gemm(map, p, d->num_sms, st);
         if (e == cudaSuccess && k_splits > 1)
             e = awq::launch_splitk_reduce(p.ws_partial, k_splits, M, N, Y, ldy, d->num_sms, st);
+        if (e == cudaSuccess && p.sk_tiles > 0) e = awq::launch_sk_fixup(p, st);
     }
     return e == cudaSuccess ? AWQ_OK : cuda_fail(e);
 }

@@ -118,6 +118,14 @@ struct TcParams {
     // zeros before the previous kernel in the stream has completed (that
     // kernel writes none of them)
     int early_w;
+    // GEMM stream-K tail (k_splits == 1, sk_tiles > 0): the first sk_full
+    // output tiles (a multiple of sk_ctas) run whole, one per CTA in turn;
+    // the K range of the last sk_tiles tiles is cut into sk_ctas equal
+    // shares of groups, one per CTA, each written as fp32 partial tiles
+    // (slots 2c, 2c + 1 of CTA c, [256 tokens][128 rows]) to ws_sk and
+    // added by launch_sk_fixup.  The grid is sk_ctas CTAs.
+    int sk_full, sk_tiles, sk_ctas;
+    float* ws_sk;
 };
 constexpr int kTcRows = 128;          // weight rows per tile (UMMA M)
 constexpr int kTcTokens = 256;        // tokens per accumulator slot (UMMA N)
@@ -129,6 +137,9 @@ cudaError_t launch_tc_gemm(const CUtensorMap& mapX, const TcParams& p, int num_s
 // Xs[m, k] = fp16(fp32(X[m, k]) * inv_s[k]) into a dense [M, K] buffer.
 cudaError_t launch_scale_x(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
                            const float* inv_s, uint16_t* Xs, int num_sms, cudaStream_t st);
+// The stream-K tail's output tiles: Y = fp16(sum of each tile's partial
+// slots in CTA order).
+cudaError_t launch_sk_fixup(const TcParams& p, cudaStream_t st);
 // Y = fp16(sum over splits of ws_partial), the splits added in order.
 cudaError_t launch_splitk_reduce(const float* ws_partial, int k_splits, int64_t M, int64_t N,
                                  uint16_t* Y, int64_t ldy, int num_sms, cudaStream_t st);

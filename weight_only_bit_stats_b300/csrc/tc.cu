@@ -96,6 +96,7 @@ constexpr size_t smem_bytes() {
 struct Item {
     int n_tile, t_tile, alpha;
     int split, g0, g1;                 // GEMM split-K: this item's groups [g0, g1)
+    int slot;                          // GEMM stream-K share: partial slot, else -1
 };
 
 template <int MODE>
@@ -139,6 +140,60 @@ __device__ __forceinline__ Item decode_item(int item, const TcParams& p) {
     return it;
 }
 
+// Stream-K tail share of CTA c (0 <= c < sk_ctas): units [s0, s1) of the
+// tail's sk_tiles * G (tile, group) units, tile-major, s_c = c * units /
+// sk_ctas.  A share is shorter than one tile's G groups, so it covers the
+// end of one tile and possibly the start of the next.
+__host__ __device__ __forceinline__ void sk_share(int c, int sk_ctas, int sk_tiles, int G,
+                                                  int64_t& s0, int64_t& s1) {
+    const int64_t units = (int64_t)sk_tiles * G;
+    s0 = (int64_t)c * units / sk_ctas;
+    s1 = (int64_t)(c + 1) * units / sk_ctas;
+}
+
+// This CTA's i-th item; false past its last.  Items go round the CTAs
+// (item blockIdx.x + i gridDim.x), except under a GEMM stream-K tail, where
+// the CTA takes whole tiles blockIdx.x + i sk_ctas of the first sk_full,
+// then its tail share (one or two pieces, partial slots 2 c and 2 c + 1).
+template <int MODE>
+__device__ __forceinline__ bool cta_item(int i, const TcParams& p, Item& it) {
+    if (is_gemm<MODE>() && p.sk_tiles > 0) {
+        const int c = blockIdx.x, nf = p.sk_full / p.sk_ctas;
+        if (i < nf) {
+            it = decode_item<MODE>(c + i * p.sk_ctas, p);
+            it.slot = -1;
+            return true;
+        }
+        int64_t s0, s1;
+        sk_share(c, p.sk_ctas, p.sk_tiles, p.G, s0, s1);
+        if (s0 >= s1) return false;
+        const int ta = (int)(s0 / p.G);
+        const int64_t a_end = min(s1, (int64_t)(ta + 1) * p.G);
+        int tile, g0, g1;
+        if (i == nf) {
+            tile = ta;
+            g0 = (int)(s0 - (int64_t)ta * p.G);
+            g1 = (int)(a_end - (int64_t)ta * p.G);
+        } else if (i == nf + 1 && s1 > a_end) {
+            tile = ta + 1;
+            g0 = 0;
+            g1 = (int)(s1 - (int64_t)(ta + 1) * p.G);
+        } else {
+            return false;
+        }
+        it = decode_item<MODE>(p.sk_full + tile, p);
+        it.g0 = g0;
+        it.g1 = g1;
+        it.slot = 2 * c + (i - nf);
+        return true;
+    }
+    const int item = blockIdx.x + i * gridDim.x;
+    if (item >= p.n_items) return false;
+    it = decode_item<MODE>(item, p);
+    it.slot = -1;
+    return true;
+}
+
 __device__ __forceinline__ uint32_t pack_h2_rn(float a, float b) {
     const __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&h);
@@ -161,8 +216,8 @@ __device__ void role_tma(const CUtensorMap* mapX, const CUtensorMap* mapA, const
     // the activation tiles are re-read by every weight tile: keep them in L2
     const uint64_t pol = l2_policy_evict_last();
     uint32_t a_iter = 0, b_iter = 0;
-    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
-        const Item it = decode_item<MODE>(item, p);
+    Item it;
+    for (int li = 0; cta_item<MODE>(li, p, it); ++li) {
         const int t0 = it.t_tile * kTcTokens * H;
         for (int g = it.g0; g < it.g1; ++g) {
             if constexpr (MODE == kModeXtX) {
@@ -212,8 +267,8 @@ __device__ void role_mma(const TcParams& p, uint8_t* As, uint8_t* Bs, SmemCtl* c
     constexpr uint32_t idesc = umma_idesc_f16_f32(kTcRows, kTcTokens);
     volatile int* abort = &ctl->abort;
     uint32_t a_iter = 0, b_iter = 0, acc_iter = 0;
-    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
-        const Item it = decode_item<MODE>(item, p);
+    Item it;
+    for (int li = 0; cta_item<MODE>(li, p, it); ++li) {
         for (int g = it.g0; g < it.g1; ++g) {
             const int sa = a_iter % kNA;
             if (!mbar_wait(&ctl->a_full[sa], (a_iter / kNA) & 1u, abort, p.status)) goto out;
@@ -297,8 +352,8 @@ __device__ void role_epilogue(const TcParams& p, SmemCtl* ctl, const GramParams*
     constexpr int H = Cfg<MODE>::kHalves;
     volatile int* abort = &ctl->abort;
     uint32_t acc_iter = 0, item_iter = 0;
-    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++item_iter) {
-        const Item it = decode_item<MODE>(item, p);
+    Item it;
+    for (int li = 0; cta_item<MODE>(li, p, it); ++li, ++item_iter) {
         const int64_t n = (int64_t)it.n_tile * kTcRows + q * 32 + lane;   // this thread's row
         const int r = q * 32 + lane;                                       // row within the tile
         float sq = 0.0f;
@@ -345,7 +400,13 @@ __device__ void role_epilogue(const TcParams& p, SmemCtl* ctl, const GramParams*
                 tmem_ld32(taddr + c * 32, v);
                 if (is_gemm<MODE>()) {
                     if (n < p.N) {
-                        if (p.k_splits == 1) {
+                        if (it.slot >= 0) {
+                            // stream-K share: fp32 partial tile [token][row]
+                            float* wsp = p.ws_sk + (int64_t)it.slot * (kTcRows * kTcTokens) +
+                                         (int64_t)(c * 32) * kTcRows + r;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) wsp[j * kTcRows] = v[j];
+                        } else if (p.k_splits == 1) {
 #pragma unroll
                             for (int j = 0; j < 32; ++j) {
                                 const int64_t tok = tok0 + c * 32 + j;
@@ -454,8 +515,8 @@ __device__ void role_prod_gemm(const TcParams& p, uint8_t* As, SmemCtl* ctl, int
     volatile int* abort = &ctl->abort;
     const int64_t wstride = p.K / 8;
     uint32_t a_iter = 0;
-    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
-        const Item it = decode_item<kModeGemm>(item, p);
+    Item it;
+    for (int li = 0; cta_item<kModeGemm>(li, p, it); ++li) {
         const int64_t n = (int64_t)it.n_tile * kTcRows + r;
         const bool valid = n < p.N;
         const uint4* qrow = reinterpret_cast<const uint4*>(p.qw + (valid ? n : 0) * wstride);
@@ -559,8 +620,8 @@ __device__ void role_prod_gemm3(const TcParams& p, uint8_t* As, SmemCtl* ctl, in
     volatile int* abort = &ctl->abort;
     const int64_t wstride = p.K / 32 * 3;                // plane words per row
     uint32_t a_iter = 0;
-    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
-        const Item it = decode_item<kModeGemm3>(item, p);
+    Item it;
+    for (int li = 0; cta_item<kModeGemm3>(li, p, it); ++li) {
         const int64_t n = (int64_t)it.n_tile * kTcRows + r;
         const bool valid = n < p.N;
         const uint4* prow = reinterpret_cast<const uint4*>(p.planes + (valid ? n : 0) * wstride);
@@ -634,28 +695,75 @@ __device__ void role_prod_gemm3(const TcParams& p, uint8_t* As, SmemCtl* ctl, in
 // 96+8c..), 32 channels in all, so the group's range takes two shuffle
 // rounds and each lane forms the group parameters once per 32 elements.  A
 // warp covers 8 rows, the 16 producer warps the 128-row tile in one pass.
-// The levels are the packer's (same rounding points), computed with the fast
-// exact quotient; E = (q - z) scale / s - W is formed as
-// ((q - z) scale - w') (1/s): the FFMA rounds (q - z) scale - w' once, and
-// (q - z) scale is exact (at most 4 + 11 significant bits), so this is the
-// value of one fp32 subtraction; times 1/s and rounded to fp16.
-__device__ __forceinline__ void unpack8(uint4 v, float4 sa, float4 sb, float* wp) {
-    const __half2* h = reinterpret_cast<const __half2*>(&v);
-    const float2 f0 = __half22float2(h[0]), f1 = __half22float2(h[1]);
-    const float2 f2 = __half22float2(h[2]), f3 = __half22float2(h[3]);
-    wp[0] = __fmul_rn(f0.x, sa.x);
-    wp[1] = __fmul_rn(f0.y, sa.y);
-    wp[2] = __fmul_rn(f1.x, sa.z);
-    wp[3] = __fmul_rn(f1.y, sa.w);
-    wp[4] = __fmul_rn(f2.x, sb.x);
-    wp[5] = __fmul_rn(f2.y, sb.y);
-    wp[6] = __fmul_rn(f3.x, sb.z);
-    wp[7] = __fmul_rn(f3.y, sb.w);
-}
-
+//
+// The lane keeps -w' = -fp32(W s) (the fp16 sign flipped before the
+// product, so exactly the negated product) as 16 pairs; the pair operations
+// round each lane as the scalar ones do.  The levels are the packer's (same
+// rounding points): with t = fp32(w' / d) by the fast exact quotient, the
+// level offset (q - z) = rint(clamp(t, -z, qmax - z)) (clamping before or
+// after rounding agree, the bounds being integers) is y - 1.5 * 2^23 with y =
+// fp32(t + 1.5 * 2^23).  When rint(lo / d) and rint(hi / d) already fall in
+// [-z, qmax - z] for every row of the warp, no t of the group leaves the
+// range and the clamp is skipped.  A chunk whose quotient comes near a tie
+// for any lane of the warp is redone with the exact quotient.
+// E = (q - z) scale / s - W is formed as ((q - z) scale - w') (1/s): the FMA
+// rounds (q - z) scale - w' once, and (q - z) scale is exact (at most 4 + 11
+// significant bits), so this is the value of one fp32 subtraction; times 1/s
+// and rounded to fp16.
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     const __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// -w' for the 8 channels of one 16-byte chunk of W, as 4 pairs.
+__device__ __forceinline__ void unpack8_neg(uint4 v, float4 sa, float4 sb, float2* wn) {
+    const uint32_t h[4] = {v.x ^ 0x80008000u, v.y ^ 0x80008000u, v.z ^ 0x80008000u,
+                           v.w ^ 0x80008000u};
+    const float2 s[4] = {make_float2(sa.x, sa.y), make_float2(sa.z, sa.w),
+                         make_float2(sb.x, sb.y), make_float2(sb.z, sb.w)};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        wn[j] = __fmul2_rn(__half22float2(*reinterpret_cast<const __half2*>(&h[j])), s[j]);
+}
+
+// The level offsets (q - z) of one chunk (4 pairs of -w'), and whether any
+// of its quotients came near a tie.
+template <bool CLAMP>
+__device__ __forceinline__ bool chunk_levels(const float2* wn, float2 nrcp2, float lo_z, float hi_z,
+                                             float2* rt) {
+    const float kM = 12582912.0f;               // 1.5 * 2^23
+    const float2 m2 = make_float2(kM, kM), negm2 = make_float2(-kM, -kM);
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
+    float dm = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float2 t = __fmul2_rn(wn[j], nrcp2);    // (-w') (-1/d)
+        if (CLAMP) {
+            t.x = fminf(fmaxf(t.x, lo_z), hi_z);
+            t.y = fminf(fmaxf(t.y, lo_z), hi_z);
+        }
+        rt[j] = __fadd2_rn(__fadd2_rn(t, m2), negm2);
+        const float2 d = __ffma2_rn(rt[j], neg1, t);
+        dm = fmax3_nan(dm, fabsf(d.x), fabsf(d.y));
+    }
+    return dm > kTieBand;
+}
+
+// The exact-quotient redo of one chunk: near-tie values take rint of the
+// IEEE quotient, clamped.
+__device__ __forceinline__ void chunk_levels_exact(const float2* wn, float scale, float rcp,
+                                                   float lo_z, float hi_z, float2* rt) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float* r = reinterpret_cast<float*>(&rt[j]);
+        const float* w = reinterpret_cast<const float*>(&wn[j]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float t = fminf(fmaxf(__fmul_rn(-w[h], rcp), lo_z), hi_z);
+            if (near_tie(t, r[h]))
+                r[h] = fminf(fmaxf(rintf(__fdiv_rn(-w[h], scale)), lo_z), hi_z);
+        }
+    }
 }
 
 template <int PW, bool GRAM>
@@ -671,8 +779,8 @@ __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, G
     const uint32_t soff0 = sw128_offset(r, 8 * c);
     uint32_t a_iter = 0, item_iter = 0;
     bool bad = false;
-    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++item_iter) {
-        const Item it = decode_item<kModeSearch>(item, p);
+    Item it;
+    for (int li = 0; cta_item<kModeSearch>(li, p, it); ++li, ++item_iter) {
         // Gram route: the groups of this item's 512 output columns, whose
         // parameters the epilogue needs (exported into buffer item_iter % 2)
         const int g_par = it.t_tile * 4;
@@ -694,22 +802,27 @@ __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, G
                 raw[q] = valid ? __ldg(reinterpret_cast<const uint4*>(wrow + kg + k))
                                : make_uint4(0, 0, 0, 0);
             }
-            // phase 1: w' = fp32(W s) for the 32 channels, and their range
-            float wp[32];
+            // phase 1: -w' for the 32 channels, and the range of w'
+            float2 wn[16];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int k = 64 * (q >> 1) + 8 * (c + 4 * (q & 1));
                 const float4* sp = reinterpret_cast<const float4*>(s_a + kg + k);
-                unpack8(raw[q], __ldg(sp), __ldg(sp + 1), wp + 8 * q);
+                unpack8_neg(raw[q], __ldg(sp), __ldg(sp + 1), wn + 4 * q);
             }
-            float lo = fmin3_nan(wp[0], wp[1], wp[2]), hi = fmax3_nan(wp[0], wp[1], wp[2]);
+            float mn[4], mx[4];                 // four independent chains over -w'
 #pragma unroll
-            for (int e = 3; e < 31; e += 2) {
-                lo = fmin3_nan(lo, wp[e], wp[e + 1]);
-                hi = fmax3_nan(hi, wp[e], wp[e + 1]);
+            for (int q = 0; q < 4; ++q) {
+                mn[q] = fmin_nan(wn[q].x, wn[q].y);
+                mx[q] = fmax_nan(wn[q].x, wn[q].y);
             }
-            lo = fmin_nan(lo, wp[31]);
-            hi = fmax_nan(hi, wp[31]);
+#pragma unroll
+            for (int e = 4; e < 16; ++e) {
+                mn[e & 3] = fmin3_nan(mn[e & 3], wn[e].x, wn[e].y);
+                mx[e & 3] = fmax3_nan(mx[e & 3], wn[e].x, wn[e].y);
+            }
+            float lo = -fmax_nan(fmax3_nan(mx[0], mx[1], mx[2]), mx[3]);
+            float hi = -fmin_nan(fmin3_nan(mn[0], mn[1], mn[2]), mn[3]);
             // this lane's 32 values: NaN or Inf makes lo or hi non-finite
             bad |= !(isfinite(lo) && isfinite(hi));
 #pragma unroll
@@ -724,7 +837,11 @@ __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, G
                 gp->rcp[g - g_par][r] = gq.rcp;
                 gp->zf[g - g_par][r] = gq.zf;
             }
-            const float neg_z = -gq.zf, top_z = p.qmax - gq.zf;
+            const float lo_z = -gq.zf, hi_z = p.qmax - gq.zf;
+            const bool inside = __all_sync(0xffffffffu,
+                                           rint_small(__fmul_rn(lo, gq.rcp)) >= lo_z &&
+                                               rint_small(__fmul_rn(hi, gq.rcp)) <= hi_z);
+            const float2 nrcp2 = make_float2(-gq.rcp, -gq.rcp), sc2 = make_float2(gq.scale, gq.scale);
             const int st = a_iter % kNA;
             if (!mbar_wait(&ctl->a_empty[st], ((a_iter / kNA) & 1u) ^ 1u, abort, p.status)) return;
             uint8_t* tile = As + st * kAStage;
@@ -734,17 +851,19 @@ __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, G
                 const int k = 64 * (q >> 1) + 8 * (c + 4 * (q & 1));
                 const float4 i0 = __ldg(reinterpret_cast<const float4*>(is_a + kg + k));
                 const float4 i1 = __ldg(reinterpret_cast<const float4*>(is_a + kg + k + 4));
-                const float is[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
-                float e[8];
-                rint_quot8(wp + 8 * q, gq.scale, gq.rcp, e);
+                const float2 is2[4] = {make_float2(i0.x, i0.y), make_float2(i0.z, i0.w),
+                                       make_float2(i1.x, i1.y), make_float2(i1.z, i1.w)};
+                float2 rt[4];
+                const bool tie = inside ? chunk_levels<false>(wn + 4 * q, nrcp2, lo_z, hi_z, rt)
+                                        : chunk_levels<true>(wn + 4 * q, nrcp2, lo_z, hi_z, rt);
+                if (__any_sync(0xffffffffu, tie))
+                    chunk_levels_exact(wn + 4 * q, gq.scale, gq.rcp, lo_z, hi_z, rt);
                 uint32_t o[4];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float qz = fminf(fmaxf(e[j], neg_z), top_z);     // (q - z)
-                    e[j] = __fmul_rn(__fmaf_rn(qz, gq.scale, -wp[8 * q + j]), is[j]);
+                for (int j = 0; j < 4; ++j) {
+                    const float2 ev = __fmul2_rn(__ffma2_rn(rt[j], sc2, wn[4 * q + j]), is2[j]);
+                    o[j] = pack_h2(ev.x, ev.y);
                 }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) o[j] = pack_h2(e[2 * j], e[2 * j + 1]);
                 const uint32_t off = (uint32_t)((q >> 1) * kASub) + ((q & 1) ? (soff0 ^ 64u) : soff0);
                 *reinterpret_cast<uint4*>(tile + off) = make_uint4(o[0], o[1], o[2], o[3]);
             }
@@ -873,7 +992,66 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// The stream-K tail's fixup: block (x, t) adds, for tail tile t, 1024
+// consecutive elements (4 per thread, [token][row] order) of the tile's
+// partial slots in CTA order (ascending groups) and rounds them to fp16 into
+// Y.  The tile's slot list is formed once per block.
+constexpr int kSkFixThreads = 256;
+constexpr int kSkFixElems = 4 * kSkFixThreads;
+constexpr int kSkMaxSlots = 512;
+
+__global__ void __launch_bounds__(kSkFixThreads) sk_fixup_kernel(const TcParams p) {
+    constexpr int kTileElems = kTcRows * kTcTokens;
+    __shared__ int slots[kSkMaxSlots];
+    __shared__ int n_slots;
+    const int t = blockIdx.y;
+    if (threadIdx.x == 0) {
+        // the CTAs whose shares meet units [t G, (t + 1) G): c(u) is the CTA
+        // with s_c <= u < s_(c+1)
+        const int64_t units = (int64_t)p.sk_tiles * p.G;
+        const int64_t u0 = (int64_t)t * p.G, u1 = u0 + p.G - 1;
+        const int c0 = (int)(((u0 + 1) * p.sk_ctas + units - 1) / units) - 1;
+        const int c1 = (int)(((u1 + 1) * p.sk_ctas + units - 1) / units) - 1;
+        int k = 0;
+        for (int c = c0; c <= c1 && k < kSkMaxSlots; ++c) {
+            int64_t s0, s1;
+            sk_share(c, p.sk_ctas, p.sk_tiles, p.G, s0, s1);
+            if (s0 < s1) slots[k++] = 2 * c + (s0 / p.G == t ? 0 : 1);
+        }
+        n_slots = k;
+    }
+    __syncthreads();
+    const Item it = decode_item<kModeGemm>(p.sk_full + t, p);
+    const int off = blockIdx.x * kSkFixElems + 4 * threadIdx.x;      // token * 128 + row
+    const int64_t n = (int64_t)it.n_tile * kTcRows + (off % kTcRows);
+    const int64_t tok = (int64_t)it.t_tile * kTcTokens + off / kTcRows;
+    if (tok >= p.rows_tok) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < n_slots; ++k) {
+        const float4 v =
+            __ldcs(reinterpret_cast<const float4*>(p.ws_sk + (int64_t)slots[k] * kTileElems + off));
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+    }
+    unsigned short* y = reinterpret_cast<unsigned short*>(p.Y) + tok * p.ldy + n;
+    const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        if (n + e < p.N) y[e] = __half_as_ushort(__float2half_rn(a[e]));
+}
+
 }  // namespace
+
+cudaError_t launch_sk_fixup(const TcParams& p, cudaStream_t st) {
+    if (p.sk_tiles <= 0) return cudaSuccess;
+    // a tile's shares come from at most 2 sk_ctas CTAs (one or two pieces each)
+    if (2 * p.sk_ctas > kSkMaxSlots) return cudaErrorInvalidValue;
+    const dim3 grid(kTcRows * kTcTokens / kSkFixElems, (unsigned)p.sk_tiles);
+    sk_fixup_kernel<<<grid, kSkFixThreads, 0, st>>>(p);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_splitk_reduce(const float* ws_partial, int k_splits, int64_t M, int64_t N,
                                  uint16_t* Y, int64_t ldy, int num_sms, cudaStream_t st) {
