@@ -168,7 +168,8 @@ awq_status awq_gram(const uint16_t* Xcal, int64_t T, int64_t K, int64_t ldx, uin
  * column is multiplied by the matching residual column and summed (fp32 per
  * 32 columns, fp64 across them).  Arguments as awq_search_scale, with G from
  * awq_gram in place of the calibration tokens; workspace >=
- * awq_search_gram_workspace_size(N, K, n_alpha) bytes. */
+ * awq_search_gram_workspace_size(N, K, n_alpha) bytes, queried on the device
+ * that runs the call (it holds two 128 x 512 fp16 residual tiles per SM). */
 size_t awq_search_gram_workspace_size(int64_t N, int64_t K, int n_alpha);
 awq_status awq_search_scale_gram(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
                                  const uint16_t* G, const double* mean_abs, const double* alphas,

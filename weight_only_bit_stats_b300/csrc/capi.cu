@@ -191,6 +191,14 @@ awq_status encode_qweight_map(CUtensorMap* map, const uint32_t* qw, int64_t N, i
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Workspace layout of awq_search_scale / awq_candidate_scales.
+int current_num_sms();
+
+// The Gram-route search's residual hand-over buffers: per CTA (at most one
+// per SM) two [128 rows][512 columns] fp16 tiles.
+size_t gram_exp_bytes(int num_sms) {
+    return align256((size_t)num_sms * 2 * awq::kTcRows * awq::kSearchTokensPerItem * 2);
+}
+
 struct SearchWs {
     size_t s_alpha, inv_s, r, mm, partials, mse, total;
 };
@@ -498,7 +506,7 @@ awq_status awq_gram(const uint16_t* Xcal, int64_t T, int64_t K, int64_t ldx, uin
 
 size_t awq_search_gram_workspace_size(int64_t N, int64_t K, int n_alpha) {
     if (N <= 0 || K <= 0 || n_alpha <= 0) return 0;
-    return search_ws(N, K, K, n_alpha).total;
+    return search_ws(N, K, K, n_alpha).total + gram_exp_bytes(current_num_sms());
 }
 
 }  // extern "C"
@@ -526,6 +534,9 @@ awq_status search_gram_impl(const uint16_t* W, int64_t N, int64_t K, int64_t ldw
     DevInfo* d = nullptr;
     awq_status s = device_info(&d);
     if (s) return s;
+    // (the residual hand-over buffers scale with the device's SM count)
+    if (ws_bytes < lay.total + gram_exp_bytes(d->num_sms))
+        return fail(AWQ_ERR_WORKSPACE, "search_scale_gram: workspace missing or too small");
     cudaStream_t st = (cudaStream_t)stream;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     float* s_alpha = s_alpha_out ? s_alpha_out : reinterpret_cast<float*>(ws + lay.s_alpha);
@@ -557,6 +568,7 @@ awq_status search_gram_impl(const uint16_t* W, int64_t N, int64_t K, int64_t ldw
     p.partials = partials;
     p.status = d->status;
     p.qmax = qmax;
+    p.e_exp = reinterpret_cast<uint16_t*>(ws + lay.total);
     e = awq::launch_tc_gram_search(map, p, d->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e);
     // G already carries the 1/T of the mean: divide the sums by N only

@@ -114,6 +114,9 @@ struct TcParams {
     float qmax;
     // 3-bit GEMM: bit planes [N][K/32][3] in place of qw
     const uint32_t* planes;
+    // Gram-route search: per CTA two [128][512] fp16 buffers through which
+    // the producer hands the epilogue the residuals of an item's columns
+    uint16_t* e_exp;
     // GEMM modes: the weight producers may read qw / planes, scales and
     // zeros before the previous kernel in the stream has completed (that
     // kernel writes none of them)

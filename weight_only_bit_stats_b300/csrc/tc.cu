@@ -66,14 +66,6 @@ struct Cfg {
     static constexpr int kHalves = is_gemm<MODE>() ? 1 : 2;     // accumulators per item
 };
 
-// Group parameters the Gram-search producer exports for the epilogue: for
-// the four groups of an item's 512 output columns, per tile row, the fp16
-// scale (as fp32), its reciprocal and the zero-point.  Two buffers (items
-// alternate).
-struct GramParams {
-    float scale[4][kTcRows], rcp[4][kTcRows], zf[4][kTcRows];
-};
-
 struct SmemCtl {
     uint64_t a_full[kNA], a_empty[kNA];
     uint64_t b_full[kNB], b_empty[kNB];
@@ -84,13 +76,12 @@ struct SmemCtl {
     int abort;
 };
 
-// Shared memory per mode: the Gram route's parameter buffers only where they
-// are used, so the other modes keep more of the SM's L1 (the GEMM producer's
-// packed-word loads and the search producer's scale loads go through it).
+// Shared memory per mode (the rest of the SM's 228 KB stays L1, which the
+// GEMM producer's packed-word loads and the search producer's scale loads
+// go through).
 template <int MODE>
 constexpr size_t smem_bytes() {
-    return 1024 /*align slack*/ + (size_t)kNA * kAStage + (size_t)kNB * kBStage +
-           (MODE == kModeGram ? 2 * sizeof(GramParams) : 0) + sizeof(SmemCtl);
+    return 1024 /*align slack*/ + (size_t)kNA * kAStage + (size_t)kNB * kBStage + sizeof(SmemCtl);
 }
 
 struct Item {
@@ -310,45 +301,9 @@ out:
     mbar_drain(&ctl->mma_done, 0);
 }
 
-// Sum over 8 consecutive channels k0..k0+7 of one group of v[j] E[n, k0+j],
-// with the residual E of this thread's row recomputed from W, s, 1/s and the
-// group's exported parameters with the producer's arithmetic (so the fp16
-// values are the ones the tensor cores multiplied).  All 32 lanes call it
-// together (the exact-quotient vote).
-__device__ __forceinline__ float gram_dot8(const TcParams& p, const float* s_a, const float* is_a,
-                                           const uint16_t* wr, bool valid, int64_t k0, float scale,
-                                           float rcp, float neg_z, float top_z, const float* v) {
-    const uint4 raw = valid ? __ldg(reinterpret_cast<const uint4*>(wr + k0)) : make_uint4(0, 0, 0, 0);
-    const float4* sp = reinterpret_cast<const float4*>(s_a + k0);
-    const float4 s0 = __ldg(sp), s1 = __ldg(sp + 1);
-    const __half2* hh = reinterpret_cast<const __half2*>(&raw);
-    const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-    float wp[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float2 f = __half22float2(hh[j]);
-        wp[2 * j] = __fmul_rn(f.x, sv[2 * j]);
-        wp[2 * j + 1] = __fmul_rn(f.y, sv[2 * j + 1]);
-    }
-    float r8[8];
-    rint_quot8(wp, scale, rcp, r8);
-    const float4* ip = reinterpret_cast<const float4*>(is_a + k0);
-    const float4 i0 = __ldg(ip), i1 = __ldg(ip + 1);
-    const float iv[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
-    float acc = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float qz = fminf(fmaxf(r8[j], neg_z), top_z);
-        const float ev = __fmul_rn(__fmaf_rn(qz, scale, -wp[j]), iv[j]);
-        acc = fmaf(v[j], __half2float(__float2half_rn(ev)), acc);
-    }
-    return acc;
-}
-
 // ---- role: epilogue ----
 template <int MODE>
-__device__ void role_epilogue(const TcParams& p, SmemCtl* ctl, const GramParams* gpar,
-                              uint32_t tmem, int q, int lane) {
+__device__ void role_epilogue(const TcParams& p, SmemCtl* ctl, uint32_t tmem, int q, int lane) {
     constexpr int H = Cfg<MODE>::kHalves;
     volatile int* abort = &ctl->abort;
     uint32_t acc_iter = 0, item_iter = 0;
@@ -358,7 +313,6 @@ __device__ void role_epilogue(const TcParams& p, SmemCtl* ctl, const GramParams*
         const int r = q * 32 + lane;                                       // row within the tile
         float sq = 0.0f;
         double dsum = 0.0;
-        const GramParams* gp = gpar + (item_iter & 1);
         for (int h = 0; h < H; ++h) {
             const int slot = acc_iter & 1;
             if (!mbar_wait(&ctl->acc_full[slot], (acc_iter >> 1) & 1u, abort, p.status)) return;
@@ -374,25 +328,35 @@ __device__ void role_epilogue(const TcParams& p, SmemCtl* ctl, const GramParams*
             for (int c = 0; c < kTcTokens / 32; ++c) {
                 if constexpr (MODE == kModeGram) {
                     // sum over these 32 columns of (E (G/T))[n, col] E[n, col],
-                    // 8 accumulator columns at a time
+                    // E being the fp16 residuals the producer exported for
+                    // this item's columns (the values the tensor cores
+                    // multiplied), 8 columns at a time
                     const int64_t col = tok0 + c * 32;
                     if (col < p.K) {                           // uniform over the warp
-                        const int gl = (int)(col / kGroup) - it.t_tile * 4;
-                        const float scale = gp->scale[gl][r], rcp = gp->rcp[gl][r];
-                        const float zf = gp->zf[gl][r];
-                        const bool valid = n < p.N;
-                        const uint16_t* wr = p.W + (valid ? n : 0) * p.ldw;
-                        const float* s_a = p.s_alpha + (int64_t)it.alpha * p.K;
-                        const float* is_a = p.inv_s_alpha + (int64_t)it.alpha * p.K;
+                        const uint4* er = reinterpret_cast<const uint4*>(
+                            p.e_exp +
+                            ((int64_t)(blockIdx.x * 2 + (item_iter & 1)) * kTcRows + r) *
+                                kSearchTokensPerItem +
+                            (col - (int64_t)it.t_tile * kSearchTokensPerItem));
+                        uint4 e4[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) e4[j] = __ldcg(er + j);
+                        float v[32];
+                        tmem_ld32(taddr + c * 32, v);
                         float acc = 0.0f;
-#pragma unroll 1
+#pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            float v8[8];
-                            tmem_ld8(taddr + c * 32 + 8 * j, v8);
-                            acc += gram_dot8(p, s_a, is_a, wr, valid, col + 8 * j, scale, rcp, -zf,
-                                             p.qmax - zf, v8);
+                            const __half2* hh = reinterpret_cast<const __half2*>(&e4[j]);
+                            float a8 = 0.0f;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = __half22float2(hh[e]);
+                                a8 = fmaf(v[8 * j + 2 * e], f.x, a8);
+                                a8 = fmaf(v[8 * j + 2 * e + 1], f.y, a8);
+                            }
+                            acc += a8;
                         }
-                        if (valid) dsum += (double)acc;
+                        if (n < p.N) dsum += (double)acc;
                     }
                     continue;
                 }
@@ -767,8 +731,7 @@ __device__ __forceinline__ void chunk_levels_exact(const float2* wn, float scale
 }
 
 template <int PW, bool GRAM>
-__device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, GramParams* gpar,
-                                 int pw, int lane) {
+__device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, int pw, int lane) {
     static_assert(PW * 8 == kTcRows, "16 producer warps x 8 rows");
     volatile int* abort = &ctl->abort;
     const int rr = lane >> 2, c = lane & 3;
@@ -782,9 +745,13 @@ __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, G
     Item it;
     for (int li = 0; cta_item<kModeSearch>(li, p, it); ++li, ++item_iter) {
         // Gram route: the groups of this item's 512 output columns, whose
-        // parameters the epilogue needs (exported into buffer item_iter % 2)
+        // residuals the epilogue needs (exported into this CTA's buffer
+        // item_iter % 2, [128 rows][512 columns] fp16)
         const int g_par = it.t_tile * 4;
-        GramParams* gp = gpar + (item_iter & 1);
+        uint16_t* e_row = GRAM ? p.e_exp +
+                                     ((int64_t)(blockIdx.x * 2 + (item_iter & 1)) * kTcRows + r) *
+                                         kSearchTokensPerItem
+                               : nullptr;
         if (GRAM && !mbar_wait(&ctl->par_empty[item_iter & 1], ((item_iter >> 1) & 1u) ^ 1u, abort,
                                p.status))
             return;
@@ -832,11 +799,6 @@ __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, G
             }
             const GroupQuant gq = group_quant_from_range(lo, hi, p.qmax);
             bad |= !gq.finite;
-            if (GRAM && c == 0 && g >= g_par && g < g_par + 4) {
-                gp->scale[g - g_par][r] = gq.scale;
-                gp->rcp[g - g_par][r] = gq.rcp;
-                gp->zf[g - g_par][r] = gq.zf;
-            }
             const float lo_z = -gq.zf, hi_z = p.qmax - gq.zf;
             const bool inside = __all_sync(0xffffffffu,
                                            rint_small(__fmul_rn(lo, gq.rcp)) >= lo_z &&
@@ -866,6 +828,9 @@ __device__ void role_prod_search(const TcParams& p, uint8_t* As, SmemCtl* ctl, G
                 }
                 const uint32_t off = (uint32_t)((q >> 1) * kASub) + ((q & 1) ? (soff0 ^ 64u) : soff0);
                 *reinterpret_cast<uint4*>(tile + off) = make_uint4(o[0], o[1], o[2], o[3]);
+                if (GRAM && g >= g_par && g < g_par + 4)
+                    *reinterpret_cast<uint4*>(e_row + (g - g_par) * kGroup + k) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -889,9 +854,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* As = smem;
     uint8_t* Bs = smem + kNA * kAStage;
-    GramParams* gpar = reinterpret_cast<GramParams*>(Bs + kNB * kBStage);
-    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(Bs + kNB * kBStage +
-                                              (MODE == kModeGram ? 2 * sizeof(GramParams) : 0));
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(Bs + kNB * kBStage);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -936,18 +899,16 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     } else if (warp == kWarpMma) {
         if (lane == 0) role_mma<MODE>(p, As, Bs, ctl, tmem);
     } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
-        role_epilogue<MODE>(p, ctl, gpar, tmem, warp - kWarpEpi0, lane);
+        role_epilogue<MODE>(p, ctl, tmem, warp - kWarpEpi0, lane);
     } else if (warp >= kWarpProd0) {
         if constexpr (MODE == kModeGemm)
             role_prod_gemm(p, As, ctl, (warp - kWarpProd0) * 32 + lane, lane);
         else if constexpr (MODE == kModeGemm3)
             role_prod_gemm3(p, As, ctl, (warp - kWarpProd0) * 32 + lane, lane);
         else if constexpr (MODE == kModeSearch)
-            role_prod_search<Cfg<MODE>::kProdWarps, false>(p, As, ctl, gpar, warp - kWarpProd0,
-                                                           lane);
+            role_prod_search<Cfg<MODE>::kProdWarps, false>(p, As, ctl, warp - kWarpProd0, lane);
         else if constexpr (MODE == kModeGram)
-            role_prod_search<Cfg<MODE>::kProdWarps, true>(p, As, ctl, gpar, warp - kWarpProd0,
-                                                          lane);
+            role_prod_search<Cfg<MODE>::kProdWarps, true>(p, As, ctl, warp - kWarpProd0, lane);
     }
 
     tc_fence_before();
