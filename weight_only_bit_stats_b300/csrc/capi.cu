@@ -140,50 +140,64 @@ awq_status make_map_rows(CUtensorMap* map, const uint16_t* X, int64_t rows, int6
     return AWQ_OK;
 }
 
-// Packed weights [N, K/8] uint32 for the decode kernel: unswizzled boxes of
-// 48 words (three groups of 128 nibbles) x 16 rows, landing as
-// [16 rows][192 B].  A decode step calls the same few weights over and over,
-// so the encoded maps are kept in a small per-thread cache keyed on
-// (address, N, K) -- a map holds nothing else -- and the encode (driver work
-// on the launch path) runs once per weight.
+// Packed weights [N, K/8] uint32 as TMA boxes.  kQwDecode: unswizzled boxes
+// of 48 words (three groups of 128 nibbles) x 16 rows for the decode kernel,
+// landing as [16 rows][192 B].  kQwGemm: one group (16 words) x 128 rows for
+// the tensor-core GEMM's producers, 64-byte swizzle (chunk j of row r lands
+// at 64 r + 16 (j ^ ((r >> 1) & 3)), so a quarter warp reading one chunk of
+// eight rows hits eight bank groups).  Matmuls are called on the same few
+// weights over and over, so the encoded maps are kept in a small per-thread
+// cache keyed on (address, N, K, kind) -- a map holds nothing else -- and
+// the encode (driver work on the launch path) runs once per weight.
+enum QwMapKind { kQwDecode = 0, kQwGemm = 1 };
 struct QwMapEntry {
     const uint32_t* qw = nullptr;
     int64_t N = 0, K = 0;
+    int kind = 0;
     CUtensorMap map;
 };
 constexpr int kQwMapCache = 16;
 thread_local QwMapEntry t_qw_maps[kQwMapCache];
 thread_local int t_qw_next = 0;
 
-awq_status encode_qweight_map(CUtensorMap* map, const uint32_t* qw, int64_t N, int64_t K);
+awq_status encode_qweight_map(CUtensorMap* map, const uint32_t* qw, int64_t N, int64_t K,
+                              int kind);
 
-awq_status make_qweight_map(CUtensorMap* map, const uint32_t* qw, int64_t N, int64_t K) {
+awq_status make_qweight_map(CUtensorMap* map, const uint32_t* qw, int64_t N, int64_t K,
+                            int kind = kQwDecode) {
     for (const QwMapEntry& e : t_qw_maps)
-        if (e.qw == qw && e.N == N && e.K == K) {
+        if (e.qw == qw && e.N == N && e.K == K && e.kind == kind) {
             *map = e.map;
             return AWQ_OK;
         }
-    awq_status s = encode_qweight_map(map, qw, N, K);
+    awq_status s = encode_qweight_map(map, qw, N, K, kind);
     if (s) return s;
     QwMapEntry& e = t_qw_maps[t_qw_next];
     t_qw_next = (t_qw_next + 1) % kQwMapCache;
     e.qw = qw;
     e.N = N;
     e.K = K;
+    e.kind = kind;
     e.map = *map;
     return AWQ_OK;
 }
 
-awq_status encode_qweight_map(CUtensorMap* map, const uint32_t* qw, int64_t N, int64_t K) {
+awq_status encode_qweight_map(CUtensorMap* map, const uint32_t* qw, int64_t N, int64_t K,
+                              int kind) {
     if (!load_encoder()) return fail(AWQ_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
     cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)N};
     cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
     cuuint32_t box[2] = {48, 16};
+    CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE;
+    if (kind == kQwGemm) {
+        box[0] = AWQ_GROUP / 8;
+        box[1] = (cuuint32_t)awq::kTcRows;
+        swz = CU_TENSOR_MAP_SWIZZLE_64B;
+    }
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(qw), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(AWQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (qweight)");
     return AWQ_OK;
 }
@@ -827,8 +841,10 @@ awq_status gemm_impl(const char* name, const uint16_t* X, int64_t M, int64_t K, 
             Xa = Xs;
             lda = K;
         }
-        CUtensorMap map;
+        CUtensorMap map, mapW;
         s = make_act_map(&map, Xa, M, K, lda);
+        if (s) return s;
+        s = make_qweight_map(&mapW, qweight, N, K, kQwGemm);
         if (s) return s;
         awq::TcParams p = {};
         p.N = (int)N;
@@ -856,7 +872,7 @@ awq_status gemm_impl(const char* name, const uint16_t* X, int64_t M, int64_t K, 
         // be read early; otherwise only when the caller allows it
         p.early_w = inv_s ? 1 : g_early_weights.load(std::memory_order_relaxed);
         if (k_splits > 1) p.ws_partial = reinterpret_cast<float*>(ws + xs_bytes);
-        e = awq::launch_tc_gemm(map, p, d->num_sms, st);
+        e = awq::launch_tc_gemm(map, mapW, p, d->num_sms, st);
         if (e == cudaSuccess && k_splits > 1)
             e = awq::launch_splitk_reduce(p.ws_partial, k_splits, M, N, Y, ldy, d->num_sms, st);
         if (e == cudaSuccess && p.sk_tiles > 0) e = awq::launch_sk_fixup(p, st);

@@ -45,13 +45,16 @@ enum { kModeGemm = 0, kModeSearch = 1, kModeXtX = 2, kModeGram = 3, kModeGemm3 =
 
 constexpr int kNA = 2;                            // A (weight) stages
 constexpr int kNB = 2;                            // B (activation) stages
+constexpr int kNW = 3;                            // GEMM packed-word stages
+constexpr int kWStage = kTcRows * 64;             // 8 KB: one group of 128 packed rows
 constexpr int kAStage = kTcRows * kGroup * 2;     // 32 KB
 constexpr int kASub = kTcRows * 64 * 2;           // 16 KB
 constexpr int kBStage = kTcTokens * kGroup * 2;   // 64 KB
 constexpr int kBSub = kTcTokens * 64 * 2;         // 32 KB
 constexpr int kTmemCols = 512;
 
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpTmem = 2, kWarpEpi0 = 4, kWarpProd0 = 8;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpTmem = 2, kWarpTmaW = 3, kWarpEpi0 = 4,
+              kWarpProd0 = 8;
 
 // The two W4A16 / W3A16 GEMM modes share everything but the producer.
 template <int MODE>
@@ -67,6 +70,7 @@ struct Cfg {
 };
 
 struct SmemCtl {
+    uint64_t w_full[kNW], w_empty[kNW];     // GEMM: packed-word ring
     uint64_t a_full[kNA], a_empty[kNA];
     uint64_t b_full[kNB], b_empty[kNB];
     uint64_t acc_full[2], acc_empty[2];
@@ -80,8 +84,13 @@ struct SmemCtl {
 // GEMM producer's packed-word loads and the search producer's scale loads
 // go through).
 template <int MODE>
+constexpr size_t ring_w_bytes() {
+    return MODE == kModeGemm ? (size_t)kNW * kWStage : 0;
+}
+template <int MODE>
 constexpr size_t smem_bytes() {
-    return 1024 /*align slack*/ + (size_t)kNA * kAStage + (size_t)kNB * kBStage + sizeof(SmemCtl);
+    return 1024 /*align slack*/ + (size_t)kNA * kAStage + (size_t)kNB * kBStage +
+           ring_w_bytes<MODE>() + sizeof(SmemCtl);
 }
 
 struct Item {
@@ -248,6 +257,35 @@ drain:
             const uint32_t i = a_iter - d;
             mbar_drain(&ctl->a_full[i % kNA], (i / kNA) & 1u);
         }
+    }
+}
+
+// ---- role: packed-weight TMA (GEMM) ----
+// One box per (item, group): the group's 16 packed words of the tile's 128
+// rows (rows past N read as zero), 64-byte swizzle, into the kNW-stage ring
+// the producer warps dequantise from.
+__device__ void role_tma_w(const CUtensorMap* mapW, const TcParams& p, uint8_t* Ws,
+                           SmemCtl* ctl) {
+    volatile int* abort = &ctl->abort;
+    uint32_t w_iter = 0;
+    Item it;
+    for (int li = 0; cta_item<kModeGemm>(li, p, it); ++li) {
+        for (int g = it.g0; g < it.g1; ++g) {
+            const int st = w_iter % kNW;
+            if (!mbar_wait(&ctl->w_empty[st], ((w_iter / kNW) & 1u) ^ 1u, abort, p.status))
+                goto drain;
+            mbar_arrive_expect_tx(&ctl->w_full[st], kWStage);
+            tma_load_2d(Ws + st * kWStage, mapW, &ctl->w_full[st], g * (kGroup / 8),
+                        it.n_tile * kTcRows);
+            ++w_iter;
+        }
+    }
+    return;
+drain:
+    // wait (bounded) for the copies this thread issued into each stage
+    for (int d = 1; d <= kNW && (int)w_iter - d >= 0; ++d) {
+        const uint32_t i = w_iter - d;
+        mbar_drain(&ctl->w_full[i % kNW], (i / kNW) & 1u);
     }
 }
 
@@ -475,43 +513,48 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr) {
 // groups cover a DRAM miss several times over.
 constexpr int kProdPrefetch = 6;
 
-__device__ void role_prod_gemm(const TcParams& p, uint8_t* As, SmemCtl* ctl, int r, int lane) {
+__device__ void role_prod_gemm(const TcParams& p, uint8_t* As, const uint8_t* Ws, SmemCtl* ctl,
+                               int r, int lane) {
     volatile int* abort = &ctl->abort;
-    const int64_t wstride = p.K / 8;
-    uint32_t a_iter = 0;
+    // this row's 16-byte chunk j of a ring stage (64-byte swizzle)
+    const uint32_t wrow = (uint32_t)r * 64u, wx = (uint32_t)((r >> 1) & 3);
+    uint32_t a_iter = 0, w_iter = 0;
     Item it;
     for (int li = 0; cta_item<kModeGemm>(li, p, it); ++li) {
         const int64_t n = (int64_t)it.n_tile * kTcRows + r;
         const bool valid = n < p.N;
-        const uint4* qrow = reinterpret_cast<const uint4*>(p.qw + (valid ? n : 0) * wstride);
         const uint16_t* srow = p.scales + (valid ? n : 0) * p.G;
         const uint16_t* zrow = p.zeros + (valid ? n : 0) * p.G;
-        uint4 cur[4];
         uint16_t csc = 0, cze = 0;
         if (valid) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) cur[j] = __ldg(qrow + (int64_t)it.g0 * 4 + j);
             csc = __ldg(srow + it.g0);
             cze = __ldg(zrow + it.g0);
-            // the row's scales and zero-points of this item, and its next
-            // groups of packed words
+            // the row's scales and zero-points of this item
             for (int g = it.g0; g < it.g1; g += 64) {
                 prefetch_l2(srow + g);
                 prefetch_l2(zrow + g);
             }
-            for (int g = it.g0 + 2; g < it.g1 && g < it.g0 + kProdPrefetch; ++g)
-                prefetch_l2(qrow + (int64_t)g * 4);
         }
         for (int g = it.g0; g < it.g1; ++g) {
-            uint4 nxt[4];
             uint16_t nsc = 0, nze = 0;
-            if (valid && g + kProdPrefetch < it.g1) prefetch_l2(qrow + (int64_t)(g + kProdPrefetch) * 4);
             if (valid && g + 1 < it.g1) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) nxt[j] = __ldg(qrow + (int64_t)(g + 1) * 4 + j);
                 nsc = __ldg(srow + g + 1);
                 nze = __ldg(zrow + g + 1);
             }
+            // the group's packed words of this row, from the TMA ring
+            const int sw = w_iter % kNW;
+            if (!mbar_wait(&ctl->w_full[sw], (w_iter / kNW) & 1u, abort, p.status)) return;
+            const uint8_t* wst = Ws + sw * kWStage + wrow;
+            uint4 cur[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                cur[j] = *reinterpret_cast<const uint4*>(wst + (((uint32_t)j ^ wx) << 4));
+            // the stage's next fill is an async-proxy write: order these
+            // generic-proxy reads before it
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->w_empty[sw]);
+            ++w_iter;
             const int st = a_iter % kNA;
             if (!mbar_wait(&ctl->a_empty[st], ((a_iter / kNA) & 1u) ^ 1u, abort, p.status)) return;
             uint8_t* tile = As + st * kAStage;
@@ -541,12 +584,8 @@ __device__ void role_prod_gemm(const TcParams& p, uint8_t* As, SmemCtl* ctl, int
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->a_full[st]);
             ++a_iter;
-            if (valid && g + 1 < it.g1) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) cur[j] = nxt[j];
-                csc = nsc;
-                cze = nze;
-            }
+            csc = nsc;
+            cze = nze;
         }
     }
 }
@@ -854,7 +893,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* As = smem;
     uint8_t* Bs = smem + kNA * kAStage;
-    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(Bs + kNB * kBStage);
+    uint8_t* Ws = Bs + kNB * kBStage;                   // GEMM: packed-word ring
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(Ws + ring_w_bytes<MODE>());
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -873,6 +913,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             mbar_init(&ctl->par_full[i], Cfg<MODE>::kProdWarps > 0 ? Cfg<MODE>::kProdWarps : 1);
             mbar_init(&ctl->par_empty[i], 4);
         }
+        for (int i = 0; i < kNW; ++i) {
+            mbar_init(&ctl->w_full[i], 1);
+            mbar_init(&ctl->w_empty[i], Cfg<MODE>::kProdWarps > 0 ? Cfg<MODE>::kProdWarps : 1);
+        }
         mbar_init(&ctl->mma_done, 1);
         ctl->abort = 0;
         fence_mbar_init();
@@ -883,7 +927,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     }
     if (warp == kWarpTma && lane == 0) {
         tma_prefetch_desc(&mapX);
-        if (MODE == kModeXtX) tma_prefetch_desc(&mapA);
+        if (MODE == kModeXtX || MODE == kModeGemm) tma_prefetch_desc(&mapA);
     }
     tc_fence_before();
     __syncthreads();
@@ -892,17 +936,21 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     // Launched as a programmatic dependent: the set-up above overlapped the
     // previous kernel; every role waits for its writes here, except the
     // weight producers of a GEMM whose previous kernel writes no weights.
-    if (!(is_gemm<MODE>() && p.early_w && warp >= kWarpProd0)) grid_dep_wait();
+    if (!(is_gemm<MODE>() && p.early_w &&
+          (warp >= kWarpProd0 || (MODE == kModeGemm && warp == kWarpTmaW))))
+        grid_dep_wait();
 
     if (warp == kWarpTma) {
         if (lane == 0) role_tma<MODE>(&mapX, &mapA, p, As, Bs, ctl);
     } else if (warp == kWarpMma) {
         if (lane == 0) role_mma<MODE>(p, As, Bs, ctl, tmem);
+    } else if (MODE == kModeGemm && warp == kWarpTmaW) {
+        if (lane == 0) role_tma_w(&mapA, p, Ws, ctl);
     } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
         role_epilogue<MODE>(p, ctl, tmem, warp - kWarpEpi0, lane);
     } else if (warp >= kWarpProd0) {
         if constexpr (MODE == kModeGemm)
-            role_prod_gemm(p, As, ctl, (warp - kWarpProd0) * 32 + lane, lane);
+            role_prod_gemm(p, As, Ws, ctl, (warp - kWarpProd0) * 32 + lane, lane);
         else if constexpr (MODE == kModeGemm3)
             role_prod_gemm3(p, As, ctl, (warp - kWarpProd0) * 32 + lane, lane);
         else if constexpr (MODE == kModeSearch)
@@ -1023,9 +1071,9 @@ cudaError_t launch_splitk_reduce(const float* ws_partial, int k_splits, int64_t 
     return cudaGetLastError();
 }
 
-cudaError_t launch_tc_gemm(const CUtensorMap& mapX, const TcParams& p, int num_sms,
-                           cudaStream_t st) {
-    return launch_tc<kModeGemm>(mapX, mapX, p, num_sms, st);
+cudaError_t launch_tc_gemm(const CUtensorMap& mapX, const CUtensorMap& mapW, const TcParams& p,
+                           int num_sms, cudaStream_t st) {
+    return launch_tc<kModeGemm>(mapX, mapW, p, num_sms, st);
 }
 cudaError_t launch_tc_search(const CUtensorMap& mapX, const TcParams& p, int num_sms,
                              cudaStream_t st) {
