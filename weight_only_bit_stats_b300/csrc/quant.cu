@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kPackThreads, kPackMinBlocks)
 // mse[a] = (sum of alpha a's partials) / (T N): one warp per alpha, lane-
 // strided fp64 sums added in a fixed butterfly order (deterministic); then
 // the first argmin and its candidate scales.
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(1024)
     search_finalize_kernel(const double* __restrict__ partials, int n_alpha, int64_t n_part,
                            int64_t T, int64_t N, int64_t K, const float* __restrict__ s_alpha,
                            double* __restrict__ mse, int32_t* __restrict__ best_idx,
@@ -324,6 +324,8 @@ __global__ void __launch_bounds__(256)
     for (int a = warp; a < n_alpha; a += blockDim.x >> 5) {
         const double* pa = partials + (int64_t)a * n_part;
         double acc = 0.0;
+        // loads of 8 strides in flight at a time; the adds stay in order
+#pragma unroll 8
         for (int64_t i = lane; i < n_part; i += 32) acc += pa[i];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
@@ -430,8 +432,9 @@ cudaError_t launch_pack_int3(const uint16_t* W, int64_t N, int64_t K, int64_t ld
 cudaError_t launch_search_finalize(const double* partials, int n_alpha, int64_t n_part, int64_t T,
                                    int64_t N, int64_t K, const float* s_alpha, double* mse,
                                    int32_t* best_idx, float* s_out, cudaStream_t st) {
-    search_finalize_kernel<<<1, 256, 0, st>>>(partials, n_alpha, n_part, T, N, K, s_alpha, mse,
-                                              best_idx, s_out);
+    // one warp per alpha (AWQ_MAX_ALPHAS = 64 at most, 32 warps: two rounds)
+    search_finalize_kernel<<<1, 1024, 0, st>>>(partials, n_alpha, n_part, T, N, K, s_alpha, mse,
+                                               best_idx, s_out);
     return cudaGetLastError();
 }
 

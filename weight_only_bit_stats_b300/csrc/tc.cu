@@ -1035,10 +1035,25 @@ __global__ void __launch_bounds__(kSkFixThreads) sk_fixup_kernel(const TcParams 
     const int64_t n = (int64_t)it.n_tile * kTcRows + (off % kTcRows);
     const int64_t tok = (int64_t)it.t_tile * kTcTokens + off / kTcRows;
     if (tok >= p.rows_tok) return;
+    // 8 slots' loads in flight at a time; the adds stay in slot order
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < n_slots; ++k) {
-        const float4 v =
-            __ldcs(reinterpret_cast<const float4*>(p.ws_sk + (int64_t)slots[k] * kTileElems + off));
+    const float* base = p.ws_sk + off;
+    int k = 0;
+    for (; k + 8 <= n_slots; k += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            v[u] = __ldcs(reinterpret_cast<const float4*>(base + (int64_t)slots[k + u] * kTileElems));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            acc.x += v[u].x;
+            acc.y += v[u].y;
+            acc.z += v[u].z;
+            acc.w += v[u].w;
+        }
+    }
+    for (; k < n_slots; ++k) {
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(base + (int64_t)slots[k] * kTileElems));
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
