@@ -114,7 +114,6 @@ __global__ void __launch_bounds__(NW * 32, DecCfg<NB>::kMinBlocks)
     gemv_w4a16_kernel(const __grid_constant__ CUtensorMap mapW, const GemvParams p) {
     using Cfg = DecCfg<NB>;
     static_assert(Cfg::kWarps == NW, "warp count");
-    constexpr int kDecWarps = NW;
     constexpr int kDecThreads = Cfg::kThreads;
     constexpr int kDecStages = Cfg::kStages;
     extern __shared__ uint8_t smem_raw[];
