@@ -508,9 +508,10 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 
-// Groups of packed words a producer row requests into L2 ahead of its own
-// loads (which run one group ahead): with ~0.7 us of MMA work per group, six
-// groups cover a DRAM miss several times over.
+// 3-bit GEMM producer: groups of plane words a row requests into L2 ahead of
+// its own loads (which run one group ahead): with ~0.7 us of MMA work per
+// group, six groups cover a DRAM miss several times over.  (The 4-bit
+// producer reads its words from the TMA ring instead.)
 constexpr int kProdPrefetch = 6;
 
 __device__ void role_prod_gemm(const TcParams& p, uint8_t* As, const uint8_t* Ws, SmemCtl* ctl,
