@@ -320,13 +320,15 @@ def test_tensor_core_gemm_parity(wb, orc, M, N, K):
     _gemm_check(wb, orc, N, K, M)
 
 
-@pytest.mark.parametrize("M,N,K", [(300, 384, 16384), (513, 256, 16384), (257, 9856, 2048)])
+@pytest.mark.parametrize("M,N,K", [(300, 384, 16384), (513, 256, 16384), (257, 9856, 2048),
+                                   (300, 200, 16384)])
 def test_gemm_stream_k_tail(wb, orc, M, N, K):
-    """Tile counts that leave a partial last wave on B300's 148 SMs (3 and 6
-    tiles with K = 16384; one whole wave of 148 tiles plus 6), for which the
-    K range of the last tiles is shared out over all CTAs and their fp32
-    partial tiles added afterwards: every output against the oracle, and
-    repeated calls bit-identical (the partials are added in a fixed order)."""
+    """Tile counts that leave a partial last wave on B300's 148 SMs (3, 4 and
+    6 tiles with K = 16384, one of them ragged in N; one whole wave of 148
+    tiles plus 6), for which the K range of the last tiles is shared out over
+    all CTAs and their fp32 partial tiles added afterwards: every output
+    against the oracle, and repeated calls bit-identical (the partials are
+    added in a fixed order)."""
     y = _gemm_check(wb, orc, N, K, M, seed=7)
     W, _, X, _ = sg.layer_inputs(13, 7, N, K, 0, M=M)
     rq, rs, rz = orc.pack_int4(W)
@@ -336,6 +338,14 @@ def test_gemm_stream_k_tail(wb, orc, M, N, K):
         Y = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
         wb.w4a16_gemm(x, qw, sc, ze, out=Y)
         assert np.array_equal(host(Y).view(np.uint16), y.view(np.uint16))
+    wb.sync_status()
+
+
+def test_gemm_ksplit_ragged(wb, orc):
+    """A ragged last weight tile (N = 392: rows past N come from the packed
+    words' TMA boxes as zeros) under the even split of K (8 parts on 148 SMs
+    for 8 tiles with K = 16384): every output against the oracle."""
+    _gemm_check(wb, orc, 392, 16384, 300, seed=8)
     wb.sync_status()
 
 
