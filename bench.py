@@ -49,9 +49,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # dram__bytes_write.sum summed over the four search launches of one step of
 # this workload in one ncu capture, valid only while the kernel's sources (comments aside) are the ones
 # captured.
-SEARCH_TRAFFIC = {"bytes_per_step": 105576192 + 2845184 + 38459648 + 0 + 185348352 + 188160 +
-                                    103374336 + 149248,
-                  "src_sha": "bf77707d1a3e00f5"}
+SEARCH_TRAFFIC = {"bytes_per_step": 105577728 + 2853376 + 38459904 + 0 + 185504768 + 217088 +
+                                    103340032 + 75264,
+                  "src_sha": "f2e881dd8f93b85a"}
 SEARCH_SOURCES = ("tc.cu", "common.cuh", "kernels.cuh")
 
 
@@ -220,6 +220,9 @@ def run_ours(args, rank, world):
         p["mse"] = torch.empty(N_ALPHA, dtype=torch.float64, device=dev)
         p["best"] = torch.empty(1, dtype=torch.int32, device=dev)
         p["ws"] = wb.search_workspace(N, K, T_CAL, N_ALPHA, dev)
+        p["cand"] = torch.empty((N_ALPHA, K), dtype=torch.float32, device=dev)
+        p["cws"] = torch.empty(max(16, wb.lib().awq_candidate_scales_workspace_size(K, N_ALPHA)),
+                               dtype=torch.uint8, device=dev)
         p["qw"] = torch.empty((N, K // 8), dtype=torch.int32, device=dev)
         p["sc"] = torch.empty((N, K // 128), dtype=torch.float16, device=dev)
         p["ze"] = torch.empty((N, K // 128), dtype=torch.float16, device=dev)
@@ -239,15 +242,20 @@ def run_ours(args, rank, world):
     stream = torch.cuda.current_stream()
     E = lambda: torch.cuda.Event(enable_timing=True)
 
-    def step(ev=None):
+    def step(ev=None, evc=None):
         for i, p in enumerate(projs):
             if ev: ev[i][0].record(stream)
             wb.act_stats(p["Xc"], out=p["abs"])
             if ev: ev[i][1].record(stream)
             wb.act_mean(p["abs"], T_CAL, out=p["mean"])
             if ev: ev[i][2].record(stream)
-            wb.search_scale(p["W"], p["Xc"], p["mean"], workspace=p["ws"],
-                            out=(p["s"], p["mse"], p["best"]))
+            # the search as its two steps: the candidate scales, then the
+            # search kernel on them (together what awq_search_scale runs;
+            # the events between them time the search kernel's call alone)
+            wb.candidate_scales(p["mean"], out=p["cand"], workspace=p["cws"])
+            if evc: evc[i].record(stream)
+            wb.search_mse(p["W"], p["Xc"], p["cand"], workspace=p["ws"],
+                          out=(p["s"], p["mse"], p["best"]))
             if ev: ev[i][3].record(stream)
             wb.pack_int4(p["W"], p["s"], out=(p["qw"], p["sc"], p["ze"]))
             wb.repack_int4(p["qw"], p["sc"], p["ze"], out=p["tiles"])
@@ -274,6 +282,7 @@ def run_ours(args, rank, world):
     sampler = ClockSampler(dev.index) if rank == 0 else None
     time.sleep(0.3)
     evs = [[[E() for _ in range(5)] for _ in range(5)] for _ in range(args.steps)]
+    evcs = [[E() for _ in range(4)] for _ in range(args.steps)]
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -282,7 +291,7 @@ def run_ours(args, rank, world):
     if sampler: sampler.mark_start()
     t_start.record(stream)
     for k in range(args.steps):
-        step(evs[k])
+        step(evs[k], evcs[k])
     t_end.record(stream)
     torch.cuda.synchronize()
     if sampler: sampler.mark_end()
@@ -290,14 +299,16 @@ def run_ours(args, rank, world):
         dist.barrier()
     wb.sync_status()
     total_ms = t_start.elapsed_time(t_end)
-    st = {"stats": 0.0, "mean": 0.0, "search": 0.0, "pack": 0.0, "flush": 0.0, "gemv": 0.0}
+    st = {"stats": 0.0, "mean": 0.0, "candidates": 0.0, "search": 0.0, "pack": 0.0,
+          "flush": 0.0, "gemv": 0.0}
     per_search = [0.0] * 4
     for k in range(args.steps):
         e = evs[k]
         for i in range(4):
             st["stats"] += e[i][0].elapsed_time(e[i][1])
             st["mean"] += e[i][1].elapsed_time(e[i][2])
-            d = e[i][2].elapsed_time(e[i][3])
+            st["candidates"] += e[i][2].elapsed_time(evcs[k][i])
+            d = evcs[k][i].elapsed_time(e[i][3])
             st["search"] += d
             per_search[i] += d
             st["pack"] += e[i][3].elapsed_time(e[i][4])
@@ -416,8 +427,10 @@ def run_ours(args, rank, world):
                      "traffic_note": "DRAM bytes per search launch, mean of the step's four "
                                      "(ncu); the algorithmic bytes (W and Xcal read once, "
                                      "candidate scales) are within a few percent",
-                     "timing": "CUDA events around each awq_search_scale call (includes its "
-                               "candidate-scale and final-reduction kernels)"},
+                     "timing": "CUDA events around each awq_search_mse call of the timed "
+                               "steps: the search kernel with its 1/s pre-pass and final "
+                               "reduction (the candidate scales are the separate "
+                               "'candidates' stage)"},
         "roofline_gemv": {"kernel": "gemv_tiles_kernel<1,16> (4 launches per step)", "bound": "hbm",
                           "achieved": round(gemv_gbs, 1), "peak": peaks["hbm_gbs"],
                           "unit": "GB/s", "frac": round(gemv_gbs / peaks["hbm_gbs"], 4),
@@ -437,9 +450,9 @@ def run_ours(args, rank, world):
                                                                (per_gemv[i] * 1e-3) / 1e9, 1),
                                        "read_us_alone": round(read_ms[i] * 1e3, 2)}
                            for i, p in enumerate(projs)},
-        # per projection and step: stats, mean, two candidate-scale kernels, search,
-        # finalize, pack, repack, decode
-        "gpu_launches": args.steps * 4 * 9,
+        # per projection and step: stats, mean, two candidate-scale kernels, 1/s,
+        # search, finalize, pack, repack, decode
+        "gpu_launches": args.steps * 4 * 10,
         "clocks": clocks,
     }
     if not args.no_e2e:

@@ -131,6 +131,23 @@ awq_status awq_search_scale(const uint16_t* W, int64_t N, int64_t K, int64_t ldw
                             awq_stream_t stream);
 size_t awq_search_workspace_size(int64_t N, int64_t K, int64_t T, int n_alpha);
 
+/* The search step alone, on caller-given candidate scales (the grid search
+ * of the third paragraph over any set of candidates): for each row a of
+ * s_alpha, mse[a] and the first argmin exactly as awq_search_scale computes
+ * them after its candidate step, with 1/s formed as fp32(1 / s) correctly
+ * rounded (the candidate step's rule), so candidates from
+ * awq_candidate_scales give awq_search_scale's results bit for bit.
+ *   s_alpha  [n_alpha, K] fp32 device, 16-byte aligned, each s > 0.
+ *   s_out    [K] fp32: the row of s_alpha at the best index.
+ * Other arguments as awq_search_scale (4 bits); workspace >=
+ * awq_search_mse_workspace_size(N, K, T, n_alpha) bytes. */
+awq_status awq_search_mse(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                          const uint16_t* Xcal, int64_t T, int64_t ldx, const float* s_alpha,
+                          int n_alpha, int group, float* s_out, double* mse_out,
+                          int32_t* best_idx, void* workspace, size_t ws_bytes,
+                          awq_stream_t stream);
+size_t awq_search_mse_workspace_size(int64_t N, int64_t K, int64_t T, int n_alpha);
+
 /* The same search at 3 bits (the pages evaluate 3 and 4 bits, fourth
  * paragraph): the fake quantiser is awq_pack_int3's (levels 0..7, scale =
  * fp16_rn(max(fp32(range / 7), 2^-14)), zero-point clamped to 0..7).

@@ -60,6 +60,8 @@ def test_version_and_workspace_sizes(capi):
     assert capi.awq_gram_workspace_size(300, 1024) >= 1024 * 320 * 2
     assert capi.awq_search_gram_workspace_size(4096, 4096, 20) == \
         capi.awq_search_workspace_size(4096, 4096, 4096, 20)
+    assert capi.awq_search_mse_workspace_size(12288, 4096, 512, 20) == \
+        capi.awq_search_workspace_size(12288, 4096, 512, 20)
 
 
 def test_host_argument_checks(capi):
@@ -129,6 +131,18 @@ def test_host_argument_checks(capi):
                                       base, None, base, 4096, None) == 2
     assert capi.awq_search_scale_gram(base, 8, 128, 128, base, base, alphas, 2, 128, base, None,
                                       base, None, None, 0, None) == 5
+    # search on given candidates: n_alpha range, null candidates, K % 128,
+    # misaligned candidates, workspace (all before any device call)
+    assert capi.awq_search_mse(base, 8, 128, 128, base, 4, 128, base, 65, 128, base, None, base,
+                               base, 4096, None) == 1
+    assert capi.awq_search_mse(base, 8, 128, 128, base, 4, 128, None, 2, 128, base, None, base,
+                               base, 4096, None) == 1
+    assert capi.awq_search_mse(base, 8, 100, 100, base, 4, 100, base, 2, 128, base, None, base,
+                               base, 4096, None) == 2
+    assert capi.awq_search_mse(base, 8, 128, 128, base, 4, 128, base + 4, 2, 128, base, None, base,
+                               base, 4096, None) == 3
+    assert capi.awq_search_mse(base, 8, 128, 128, base, 4, 128, base, 2, 128, base, None, base,
+                               None, 0, None) == 5
     assert capi.awq_last_error_string()
 
 

@@ -285,6 +285,26 @@ def test_search_parity_single_linear_layer(wb, orc):
     assert best > 0 and mse[best] < mse[0]
 
 
+@pytest.mark.parametrize("N,K,T", [(136, 384, 700), (1024, 1024, 512)])
+def test_search_on_given_candidates(wb, orc, N, K, T):
+    """awq_search_mse on awq_candidate_scales' candidates reproduces
+    awq_search_scale bit for bit (mse, best index, s); a custom candidate
+    set (two rows of the grid, swapped) gives those rows' mse."""
+    W, X, _, _ = sg.layer_inputs(12, 3, N, K, T)
+    Wd, Xd = dev(W), dev(X)
+    m = wb.act_mean(wb.act_stats(Xd), T)
+    s1, mse1, b1 = wb.search_scale(Wd, Xd, m)
+    cand = wb.candidate_scales(m)
+    s2, mse2, b2 = wb.search_mse(Wd, Xd, cand)
+    assert np.array_equal(host(mse1), host(mse2))
+    assert int(host(b1)[0]) == int(host(b2)[0])
+    assert np.array_equal(host(s1), host(s2))
+    pick = torch.stack([cand[7], cand[3]]).contiguous()
+    _, mse3, _ = wb.search_mse(Wd, Xd, pick)
+    assert np.array_equal(host(mse3), host(mse1)[[7, 3]])
+    wb.sync_status()
+
+
 def test_search_custom_grid(wb, orc):
     W, X, _, _ = sg.layer_inputs(12, 0, 128, 256, 40)
     _search_check(wb, orc, W, X, alphas=(0.0, 0.25, 0.5, 0.75, 1.0))

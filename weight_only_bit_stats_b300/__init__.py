@@ -83,6 +83,9 @@ SIGNATURES = (
                                      _p, _sz, _p]),
     ("awq_search_scale_gram_int3", _int, [_p, _i64, _i64, _i64, _p, _p, _p, _int, _int, _p, _p, _p,
                                           _p, _p, _sz, _p]),
+    ("awq_search_mse", _int, [_p, _i64, _i64, _i64, _p, _i64, _i64, _p, _int, _int, _p, _p, _p,
+                              _p, _sz, _p]),
+    ("awq_search_mse_workspace_size", _sz, [_i64, _i64, _i64, _int]),
     ("awq_search_scale_int3", _int, [_p, _i64, _i64, _i64, _p, _i64, _i64, _p, _p, _int, _int, _p,
                                      _p, _p, _p, _p, _sz, _p]),
     ("awq_repack_int4", _int, [_p, _p, _p, _i64, _i64, _int, _p, _sz, _p]),
@@ -171,17 +174,47 @@ def _alphas(alphas) -> tuple[ctypes.Array, int]:
     return (ctypes.c_double * len(a))(*a), len(a)
 
 
-def candidate_scales(mean_abs: torch.Tensor, alphas=ALPHA_GRID, stream=None) -> torch.Tensor:
+def candidate_scales(mean_abs: torch.Tensor, alphas=ALPHA_GRID, out: torch.Tensor | None = None,
+                     workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """All candidate scales, fp32 [n_alpha, K]."""
     _dev(mean_abs, torch.float64, "mean_abs")
     K = mean_abs.shape[0]
     arr, n = _alphas(alphas)
-    out = torch.empty((n, K), dtype=torch.float32, device=mean_abs.device)
+    if out is None:
+        out = torch.empty((n, K), dtype=torch.float32, device=mean_abs.device)
     ws_n = lib().awq_candidate_scales_workspace_size(K, n)
-    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=mean_abs.device)
+    ws = workspace if workspace is not None else \
+        torch.empty(max(ws_n, 16), dtype=torch.uint8, device=mean_abs.device)
     _check(lib().awq_candidate_scales(mean_abs.data_ptr(), K, arr, n, out.data_ptr(),
-                                      ws.data_ptr(), ws_n, _stream(stream)), "awq_candidate_scales")
+                                      ws.data_ptr(), ws.numel(), _stream(stream)),
+           "awq_candidate_scales")
     return out
+
+
+def search_mse(W: torch.Tensor, Xcal: torch.Tensor, s_alpha: torch.Tensor,
+               workspace: torch.Tensor | None = None, out=None, stream=None):
+    """The search on given candidate scales s_alpha [n_alpha, K]: returns
+    (s, mse, best) like ``search_scale``."""
+    _dev(W, torch.float16, "W")
+    _dev(Xcal, torch.float16, "Xcal")
+    _dev(s_alpha, torch.float32, "s_alpha")
+    N, K = W.shape
+    T = Xcal.shape[0]
+    na = s_alpha.shape[0]
+    if out is None:
+        s = torch.empty(K, dtype=torch.float32, device=W.device)
+        mse = torch.empty(na, dtype=torch.float64, device=W.device)
+        best = torch.empty(1, dtype=torch.int32, device=W.device)
+    else:
+        s, mse, best = out
+    n = lib().awq_search_mse_workspace_size(N, K, T, na)
+    if workspace is None:
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=W.device)
+    _check(lib().awq_search_mse(W.data_ptr(), N, K, _ld(W), Xcal.data_ptr(), T, _ld(Xcal),
+                                s_alpha.data_ptr(), na, GROUP, s.data_ptr(), mse.data_ptr(),
+                                best.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                _stream(stream)), "awq_search_mse")
+    return s, mse, best
 
 
 def search_workspace(N: int, K: int, T: int, n_alpha: int, device) -> torch.Tensor:

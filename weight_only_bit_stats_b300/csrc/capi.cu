@@ -380,6 +380,11 @@ size_t awq_search_workspace_size(int64_t N, int64_t K, int64_t T, int n_alpha) {
 namespace {
 
 // awq_search_scale and its 3-bit form: levels 0..qmax.
+awq_status search_run(DevInfo* d, const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                      const uint16_t* Xcal, int64_t T, int64_t ldx, const float* s_alpha,
+                      const float* inv_s, int n_alpha, double* partials, double* mse,
+                      int32_t* best_idx, float* s_out, cudaStream_t st, float qmax);
+
 awq_status search_impl(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, const uint16_t* Xcal,
                        int64_t T, int64_t ldx, const double* mean_abs, const double* alphas,
                        int n_alpha, int group, float* s_out, double* mse_out, int32_t* best_idx,
@@ -415,9 +420,18 @@ awq_status search_impl(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, con
                                                  reinterpret_cast<double*>(ws + lay.r),
                                                  reinterpret_cast<double*>(ws + lay.mm), st);
     if (e != cudaSuccess) return cuda_fail(e);
+    return search_run(d, W, N, K, ldw, Xcal, T, ldx, s_alpha, inv_s, n_alpha, partials, mse,
+                      best_idx, s_out, st, qmax);
+}
 
+// The tensor-core search and the final reduction on candidate scales already
+// in place (s_alpha and inv_s, [n_alpha][K] fp32); arguments checked.
+awq_status search_run(DevInfo* d, const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                      const uint16_t* Xcal, int64_t T, int64_t ldx, const float* s_alpha,
+                      const float* inv_s, int n_alpha, double* partials, double* mse,
+                      int32_t* best_idx, float* s_out, cudaStream_t st, float qmax) {
     CUtensorMap map;
-    s = make_act_map(&map, Xcal, T, K, ldx);
+    awq_status s = make_act_map(&map, Xcal, T, K, ldx);
     if (s) return s;
     awq::TcParams p = {};
     p.N = (int)N;
@@ -435,7 +449,7 @@ awq_status search_impl(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, con
     p.partials = partials;
     p.status = d->status;
     p.qmax = qmax;
-    e = awq::launch_tc_search(map, p, d->num_sms, st);
+    cudaError_t e = awq::launch_tc_search(map, p, d->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e);
     e = awq::launch_search_finalize(partials, n_alpha, (int64_t)p.n_tiles * p.t_tiles * 4, T, N, K,
                                     s_alpha, mse, best_idx, s_out, st);
@@ -454,6 +468,44 @@ awq_status awq_search_scale(const uint16_t* W, int64_t N, int64_t K, int64_t ldw
     const CallRange range("awq_search_scale");
     return search_impl(W, N, K, ldw, Xcal, T, ldx, mean_abs, alphas, n_alpha, group, s_out,
                        mse_out, best_idx, s_alpha_out, workspace, ws_bytes, stream, 15.0f);
+}
+
+size_t awq_search_mse_workspace_size(int64_t N, int64_t K, int64_t T, int n_alpha) {
+    if (N <= 0 || K <= 0 || T <= 0 || n_alpha <= 0) return 0;
+    return search_ws(N, K, T, n_alpha).total;
+}
+
+awq_status awq_search_mse(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                          const uint16_t* Xcal, int64_t T, int64_t ldx, const float* s_alpha,
+                          int n_alpha, int group, float* s_out, double* mse_out,
+                          int32_t* best_idx, void* workspace, size_t ws_bytes,
+                          awq_stream_t stream) {
+    const CallRange range("awq_search_mse");
+    if (N <= 0 || K <= 0 || T <= 0 || n_alpha < 1 || n_alpha > AWQ_MAX_ALPHAS)
+        return fail(AWQ_ERR_INVALID_ARG, "search_mse: sizes must be positive, 1 <= n_alpha <= 64");
+    if (!W || !Xcal || !s_alpha || !s_out || !best_idx)
+        return fail(AWQ_ERR_INVALID_ARG, "search_mse: null pointer");
+    if (group != AWQ_GROUP || K % AWQ_GROUP || N % 8 || ldw < K || ldx < K || ldw % 8 || ldx % 8)
+        return fail(AWQ_ERR_SHAPE, "search_mse: need group 128, K % 128 == 0, N % 8 == 0, ld >= K, ld % 8 == 0");
+    if (N > (1LL << 30) || T > (1LL << 30) || K > (1LL << 30))
+        return fail(AWQ_ERR_SHAPE, "search_mse: size too large");
+    if (!aligned16(W) || !aligned16(Xcal) || !aligned16(s_out) || !aligned16(s_alpha))
+        return fail(AWQ_ERR_ALIGN, "search_mse: W, Xcal, s_alpha, s_out must be 16-byte aligned");
+    const SearchWs lay = search_ws(N, K, T, n_alpha);
+    if (!workspace || ws_bytes < lay.total || !aligned16(workspace))
+        return fail(AWQ_ERR_WORKSPACE, "search_mse: workspace missing or too small");
+    DevInfo* d = nullptr;
+    awq_status s = device_info(&d);
+    if (s) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* inv_s = reinterpret_cast<float*>(ws + lay.inv_s);
+    double* partials = reinterpret_cast<double*>(ws + lay.partials);
+    double* mse = mse_out ? mse_out : reinterpret_cast<double*>(ws + lay.mse);
+    cudaError_t e = awq::launch_reciprocals(s_alpha, (int64_t)n_alpha * K, inv_s, d->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return search_run(d, W, N, K, ldw, Xcal, T, ldx, s_alpha, inv_s, n_alpha, partials, mse,
+                      best_idx, s_out, st, 15.0f);
 }
 
 awq_status awq_search_scale_int3(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,

@@ -139,6 +139,9 @@ constexpr int kSearchTokensPerItem = 512;
 // of one group x 128 rows, 64-byte swizzle.
 cudaError_t launch_tc_gemm(const CUtensorMap& mapX, const CUtensorMap& mapW, const TcParams& p,
                            int num_sms, cudaStream_t st);
+// inv[i] = fp32(1 / s[i]), correctly rounded, for n values.
+cudaError_t launch_reciprocals(const float* s, int64_t n, float* inv, int num_sms,
+                               cudaStream_t st);
 // Xs[m, k] = fp16(fp32(X[m, k]) * inv_s[k]) into a dense [M, K] buffer.
 cudaError_t launch_scale_x(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
                            const float* inv_s, uint16_t* Xs, int num_sms, cudaStream_t st);

@@ -348,6 +348,14 @@ __global__ void __launch_bounds__(1024)
     for (int64_t k = threadIdx.x; k < K / 4; k += blockDim.x) dst[k] = src[k];
 }
 
+// inv[i] = fp32(1 / s[i]) correctly rounded (the candidate kernel's rule).
+__global__ void __launch_bounds__(256)
+    reciprocal_kernel(const float* __restrict__ s, int64_t n, float* __restrict__ inv) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        inv[i] = __frcp_rn(s[i]);
+}
+
 // Xs = fp16(fp32(X) * inv_s), 8 activations per thread (K % 8 == 0).
 __global__ void __launch_bounds__(256)
     scale_x_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K, int64_t ldx,
@@ -384,6 +392,15 @@ unsigned pack_blocks(int64_t N, int64_t K, int num_sms) {
 }
 
 }  // namespace
+
+cudaError_t launch_reciprocals(const float* s, int64_t n, float* inv, int num_sms,
+                               cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
+    reciprocal_kernel<<<(unsigned)blocks, 256, 0, st>>>(s, n, inv);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_scale_x(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
                            const float* inv_s, uint16_t* Xs, int num_sms, cudaStream_t st) {
