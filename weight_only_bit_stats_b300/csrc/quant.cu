@@ -12,7 +12,10 @@
 namespace awq {
 namespace {
 
-constexpr int kCandThreads = 256;
+// Candidate scales: pass 1 in blocks of 64 (the fp64 pow is the work; small
+// blocks spread it evenly over the SMs), pass 2 in blocks of 256.
+constexpr int kCandThreads = 64;
+constexpr int kCand2Threads = 256;
 // Pack launch shape: 128-thread blocks held to 96 registers (five resident
 // per SM), grid capped at two waves of them.
 #ifndef AWQ_PACK_BLOCKS_PER_SM
@@ -64,22 +67,29 @@ __global__ void __launch_bounds__(kCandThreads)
 }
 
 // Pass 2: s_k = fp32(r_k / sqrt(max r * min r)); also 1/s_k (IEEE fp32).
-__global__ void __launch_bounds__(kCandThreads)
+// The first warp reduces pass 1's block extremes (max and min are exact,
+// so the order does not matter).
+__global__ void __launch_bounds__(kCand2Threads)
     cand_pass2_kernel(int64_t K, int n_blocks, const double* __restrict__ ws_r,
                       const double* __restrict__ ws_mm, float* __restrict__ s_alpha,
                       float* __restrict__ inv_s_alpha) {
     __shared__ double norm_s;
     const int a = blockIdx.y;
-    if (threadIdx.x == 0) {
+    if (threadIdx.x < 32) {
         double mx = -INFINITY, mn = INFINITY;
-        for (int b = 0; b < n_blocks; ++b) {
+        for (int b = threadIdx.x; b < n_blocks; b += 32) {
             mx = fmax(mx, ws_mm[((int64_t)a * n_blocks + b) * 2]);
             mn = fmin(mn, ws_mm[((int64_t)a * n_blocks + b) * 2 + 1]);
         }
-        norm_s = sqrt(mx * mn);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            mn = fmin(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        }
+        if (threadIdx.x == 0) norm_s = sqrt(mx * mn);
     }
     __syncthreads();
-    const int64_t k = (int64_t)blockIdx.x * kCandThreads + threadIdx.x;
+    const int64_t k = (int64_t)blockIdx.x * kCand2Threads + threadIdx.x;
     if (k < K) {
         float s = __double2float_rn(ws_r[(int64_t)a * K + k] / norm_s);
         s_alpha[(int64_t)a * K + k] = s;
@@ -417,11 +427,12 @@ int cand_blocks(int64_t K) { return (int)((K + kCandThreads - 1) / kCandThreads)
 cudaError_t launch_candidate_scales(const double* mean, int64_t K, const AlphaList& alphas,
                                     int n_alpha, float* s_alpha, float* inv_s_alpha, double* ws_r,
                                     double* ws_mm, cudaStream_t st) {
-    dim3 grid(cand_blocks(K), n_alpha);
+    const dim3 grid(cand_blocks(K), n_alpha);
     cand_pass1_kernel<<<grid, kCandThreads, 0, st>>>(mean, K, alphas, ws_r, ws_mm);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    cand_pass2_kernel<<<grid, kCandThreads, 0, st>>>(K, cand_blocks(K), ws_r, ws_mm, s_alpha,
+    const dim3 grid2((unsigned)((K + kCand2Threads - 1) / kCand2Threads), n_alpha);
+    cand_pass2_kernel<<<grid2, kCand2Threads, 0, st>>>(K, cand_blocks(K), ws_r, ws_mm, s_alpha,
                                                       inv_s_alpha);
     return cudaGetLastError();
 }
