@@ -362,18 +362,21 @@ cudaError_t launch_tiles_cfg(const TileParams& p, int grid, cudaStream_t st) {
 }
 
 // One thread per 16 bytes of the tiled buffer (68 per tile): consecutive
-// threads write consecutive bytes.
+// threads write consecutive bytes.  I is the chunk index type: 32-bit
+// whenever the chunk count fits (its divisions are several times cheaper),
+// else 64-bit.
+template <typename I>
 __global__ void __launch_bounds__(256)
     repack_int4_kernel(const uint32_t* __restrict__ qweight, const uint16_t* __restrict__ scales,
                        const uint16_t* __restrict__ zeros, int64_t N, int64_t K,
                        uint4* __restrict__ tiles, int64_t n_chunks) {
     constexpr int kChunks = kTileBytes / 16;            // 68
-    const int64_t G = K / kGroup;
-    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < n_chunks;
-         u += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t tile = u / kChunks;
+    const I G = (I)(K / kGroup);
+    for (I u = (I)blockIdx.x * blockDim.x + threadIdx.x; u < (I)n_chunks;
+         u += (I)gridDim.x * blockDim.x) {
+        const I tile = u / kChunks;
         const int c = (int)(u - tile * kChunks);
-        const int64_t j = tile / G, gi = tile - j * G;
+        const int64_t j = tile / G, gi = tile - (I)j * G;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (c < 64) {
             const int h = c >> 5, L = c & 31;
@@ -402,17 +405,19 @@ __global__ void __launch_bounds__(256)
 // The 3-bit tiles: one thread per 16 bytes (52 per tile): 48 chunks of the
 // 16 rows' planes (row r's 48 bytes at 48 r), then the four of scales and
 // zero-points.
+template <typename I>
 __global__ void __launch_bounds__(256)
     repack_int3_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restrict__ scales,
                        const uint16_t* __restrict__ zeros, int64_t N, int64_t K,
                        uint4* __restrict__ tiles, int64_t n_chunks) {
     constexpr int kChunks = kTile3Bytes / 16;           // 52
-    const int64_t G = K / kGroup, wrow = K / 32 * 3;
-    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < n_chunks;
-         u += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t tile = u / kChunks;
+    const I G = (I)(K / kGroup);
+    const int64_t wrow = K / 32 * 3;
+    for (I u = (I)blockIdx.x * blockDim.x + threadIdx.x; u < (I)n_chunks;
+         u += (I)gridDim.x * blockDim.x) {
+        const I tile = u / kChunks;
         const int c = (int)(u - tile * kChunks);
-        const int64_t j = tile / G, gi = tile - j * G;
+        const int64_t j = tile / G, gi = tile - (I)j * G;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (c < 48) {
             const int64_t row = j * kDecRows + c / 3;
@@ -445,8 +450,12 @@ cudaError_t launch_repack_int3(const uint32_t* planes, const uint16_t* scales,
     if (n_chunks == 0) return cudaSuccess;
     int64_t blocks = (n_chunks + 255) / 256;
     if (blocks > (int64_t)num_sms * 16) blocks = (int64_t)num_sms * 16;
-    repack_int3_kernel<<<(unsigned)blocks, 256, 0, st>>>(planes, scales, zeros, N, K,
-                                                         static_cast<uint4*>(tiles), n_chunks);
+    if (n_chunks + (int64_t)blocks * 256 < (1LL << 32))
+        repack_int3_kernel<uint32_t><<<(unsigned)blocks, 256, 0, st>>>(
+            planes, scales, zeros, N, K, static_cast<uint4*>(tiles), n_chunks);
+    else
+        repack_int3_kernel<int64_t><<<(unsigned)blocks, 256, 0, st>>>(
+            planes, scales, zeros, N, K, static_cast<uint4*>(tiles), n_chunks);
     return cudaGetLastError();
 }
 
@@ -470,8 +479,12 @@ cudaError_t launch_repack_int4(const uint32_t* qweight, const uint16_t* scales,
     if (n_chunks == 0) return cudaSuccess;
     int64_t blocks = (n_chunks + 255) / 256;
     if (blocks > (int64_t)num_sms * 16) blocks = (int64_t)num_sms * 16;
-    repack_int4_kernel<<<(unsigned)blocks, 256, 0, st>>>(qweight, scales, zeros, N, K,
-                                                         static_cast<uint4*>(tiles), n_chunks);
+    if (n_chunks + (int64_t)blocks * 256 < (1LL << 32))
+        repack_int4_kernel<uint32_t><<<(unsigned)blocks, 256, 0, st>>>(
+            qweight, scales, zeros, N, K, static_cast<uint4*>(tiles), n_chunks);
+    else
+        repack_int4_kernel<int64_t><<<(unsigned)blocks, 256, 0, st>>>(
+            qweight, scales, zeros, N, K, static_cast<uint4*>(tiles), n_chunks);
     return cudaGetLastError();
 }
 
