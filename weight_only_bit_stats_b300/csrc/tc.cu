@@ -1005,30 +1005,41 @@ __global__ void __launch_bounds__(256)
 // The stream-K tail's fixup: block (x, t) adds, for tail tile t, 1024
 // consecutive elements (4 per thread, [token][row] order) of the tile's
 // partial slots in CTA order (ascending groups) and rounds them to fp16 into
-// Y.  The tile's slot list is formed once per block.
+// Y.  It is launched as a programmatic dependent of the GEMM: the slot list,
+// which depends only on the schedule, is formed (by one warp, 32 CTAs at a
+// time) while the GEMM's last CTAs finish, and the partials are read after
+// griddepcontrol.wait.  kSkInFlight slots' loads are issued together; the
+// adds stay in slot order.
 constexpr int kSkFixThreads = 256;
 constexpr int kSkFixElems = 4 * kSkFixThreads;
 constexpr int kSkMaxSlots = 512;
+constexpr int kSkInFlight = 16;
 
 __global__ void __launch_bounds__(kSkFixThreads) sk_fixup_kernel(const TcParams p) {
     constexpr int kTileElems = kTcRows * kTcTokens;
     __shared__ int slots[kSkMaxSlots];
     __shared__ int n_slots;
     const int t = blockIdx.y;
-    if (threadIdx.x == 0) {
+    if (threadIdx.x < 32) {
         // the CTAs whose shares meet units [t G, (t + 1) G): c(u) is the CTA
-        // with s_c <= u < s_(c+1)
+        // with s_c <= u < s_(c+1); those with empty shares are left out
+        const int lane = threadIdx.x;
         const int64_t units = (int64_t)p.sk_tiles * p.G;
         const int64_t u0 = (int64_t)t * p.G, u1 = u0 + p.G - 1;
         const int c0 = (int)(((u0 + 1) * p.sk_ctas + units - 1) / units) - 1;
         const int c1 = (int)(((u1 + 1) * p.sk_ctas + units - 1) / units) - 1;
         int k = 0;
-        for (int c = c0; c <= c1 && k < kSkMaxSlots; ++c) {
-            int64_t s0, s1;
-            sk_share(c, p.sk_ctas, p.sk_tiles, p.G, s0, s1);
-            if (s0 < s1) slots[k++] = 2 * c + (s0 / p.G == t ? 0 : 1);
+        for (int cb = c0; cb <= c1; cb += 32) {
+            const int c = cb + lane;
+            int64_t s0 = 0, s1 = 0;
+            if (c <= c1) sk_share(c, p.sk_ctas, p.sk_tiles, p.G, s0, s1);
+            const bool has = c <= c1 && s0 < s1;
+            const unsigned m = __ballot_sync(0xffffffffu, has);
+            const int pos = k + __popc(m & ((1u << lane) - 1u));
+            if (has && pos < kSkMaxSlots) slots[pos] = 2 * c + (s0 / p.G == t ? 0 : 1);
+            k += __popc(m);
         }
-        n_slots = k;
+        if (lane == 0) n_slots = k < kSkMaxSlots ? k : kSkMaxSlots;
     }
     __syncthreads();
     const Item it = decode_item<kModeGemm>(p.sk_full + t, p);
@@ -1036,29 +1047,25 @@ __global__ void __launch_bounds__(kSkFixThreads) sk_fixup_kernel(const TcParams 
     const int64_t n = (int64_t)it.n_tile * kTcRows + (off % kTcRows);
     const int64_t tok = (int64_t)it.t_tile * kTcTokens + off / kTcRows;
     if (tok >= p.rows_tok) return;
-    // 8 slots' loads in flight at a time; the adds stay in slot order
+    grid_dep_wait();
+    const int ns = n_slots;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const float* base = p.ws_sk + off;
-    int k = 0;
-    for (; k + 8 <= n_slots; k += 8) {
-        float4 v[8];
+    for (int k = 0; k < ns; k += kSkInFlight) {
+        float4 v[kSkInFlight];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-            v[u] = __ldcs(reinterpret_cast<const float4*>(base + (int64_t)slots[k + u] * kTileElems));
+        for (int u = 0; u < kSkInFlight; ++u)
+            if (k + u < ns)
+                v[u] = __ldcs(reinterpret_cast<const float4*>(base + (int64_t)slots[k + u] * kTileElems));
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            acc.x += v[u].x;
-            acc.y += v[u].y;
-            acc.z += v[u].z;
-            acc.w += v[u].w;
+        for (int u = 0; u < kSkInFlight; ++u) {
+            if (k + u < ns) {
+                acc.x += v[u].x;
+                acc.y += v[u].y;
+                acc.z += v[u].z;
+                acc.w += v[u].w;
+            }
         }
-    }
-    for (; k < n_slots; ++k) {
-        const float4 v = __ldcs(reinterpret_cast<const float4*>(base + (int64_t)slots[k] * kTileElems));
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
     }
     unsigned short* y = reinterpret_cast<unsigned short*>(p.Y) + tok * p.ldy + n;
     const float a[4] = {acc.x, acc.y, acc.z, acc.w};
@@ -1073,9 +1080,16 @@ cudaError_t launch_sk_fixup(const TcParams& p, cudaStream_t st) {
     if (p.sk_tiles <= 0) return cudaSuccess;
     // a tile's shares come from at most 2 sk_ctas CTAs (one or two pieces each)
     if (2 * p.sk_ctas > kSkMaxSlots) return cudaErrorInvalidValue;
-    const dim3 grid(kTcRows * kTcTokens / kSkFixElems, (unsigned)p.sk_tiles);
-    sk_fixup_kernel<<<grid, kSkFixThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kTcRows * kTcTokens / kSkFixElems, (unsigned)p.sk_tiles);
+    cfg.blockDim = dim3(kSkFixThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, sk_fixup_kernel, p);
 }
 
 cudaError_t launch_splitk_reduce(const float* ws_partial, int k_splits, int64_t M, int64_t N,
