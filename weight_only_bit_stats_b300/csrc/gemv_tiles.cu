@@ -24,9 +24,10 @@
 // when N % 16 == 0), so the kernel's algorithmic traffic is unchanged, but a
 // warp's share of the matrix is now one contiguous byte range:
 //
-//  * Persistent grid, one CTA per SM; CTA c owns a balanced run of slabs,
-//    i.e. a contiguous run of tiles, and its warps split that run into equal
-//    contiguous ranges (intra-CTA split-K where a slab is shared).
+//  * Persistent grid, one CTA per SM; CTA c owns a balanced run of slabs
+//    (the runs one slab longer first), i.e. a contiguous run of tiles, and
+//    its warps split that run into equal contiguous ranges (intra-CTA
+//    split-K where a slab is shared).
 //  * Each warp streams its range through its own ring in shared memory with
 //    plain 1-D bulk copies (cp.async.bulk), three tiles per stage.  No tensor
 //    map is involved, so the host encodes nothing per call.
@@ -128,8 +129,12 @@ __global__ void __launch_bounds__(NW * 32, AWQ_TILE_MINBLOCKS) gemv_tiles_kernel
     // ---- work split: slabs over CTAs, tiles over warps ----
     // CTA-local tile indices fit in 32 bits (checked on the host).
     const int n_slabs = (int)((p.N + kDecRows - 1) / kDecRows);
-    const int s0 = (int)((int64_t)blockIdx.x * n_slabs / gridDim.x);
-    const int s1 = (int)((int64_t)(blockIdx.x + 1) * n_slabs / gridDim.x);
+    // The CTAs with one slab more come first: blocks are dispatched in index
+    // order, so in a chain of programmatic launches the next kernel's heavier
+    // CTAs take the SMs that this kernel's lighter CTAs free first.
+    const int q = n_slabs / (int)gridDim.x, r = n_slabs - q * (int)gridDim.x;
+    const int s0 = (int)blockIdx.x * q + min((int)blockIdx.x, r);
+    const int s1 = s0 + q + ((int)blockIdx.x < r ? 1 : 0);
     const int U = (s1 - s0) * G;
     const int u_lo = warp_lo<NW>(U, warp), u_hi = warp_lo<NW>(U, warp + 1);
     const int n_my = u_hi - u_lo;
