@@ -1008,14 +1008,21 @@ __global__ void __launch_bounds__(256)
 // Y.  It is launched as a programmatic dependent of the GEMM: the slot list,
 // which depends only on the schedule, is formed (by one warp, 32 CTAs at a
 // time) while the GEMM's last CTAs finish, and the partials are read after
-// griddepcontrol.wait.  kSkInFlight slots' loads are issued together; the
-// adds stay in slot order.
+// griddepcontrol.wait.  NF slots' loads are issued together and the adds
+// stay in slot order; a wider batch takes more registers, hence fewer blocks
+// per SM (the launcher picks NF from the slots per tile and the block count).
 constexpr int kSkFixThreads = 256;
 constexpr int kSkFixElems = 4 * kSkFixThreads;
 constexpr int kSkMaxSlots = 512;
-constexpr int kSkInFlight = 16;
 
-__global__ void __launch_bounds__(kSkFixThreads) sk_fixup_kernel(const TcParams p) {
+template <int NF>
+constexpr int sk_fix_blocks_per_sm() {
+    return NF >= 16 ? 2 : NF >= 8 ? 4 : 5;
+}
+
+template <int NF>
+__global__ void __launch_bounds__(kSkFixThreads, sk_fix_blocks_per_sm<NF>())
+    sk_fixup_kernel(const TcParams p) {
     constexpr int kTileElems = kTcRows * kTcTokens;
     __shared__ int slots[kSkMaxSlots];
     __shared__ int n_slots;
@@ -1051,14 +1058,14 @@ __global__ void __launch_bounds__(kSkFixThreads) sk_fixup_kernel(const TcParams 
     const int ns = n_slots;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const float* base = p.ws_sk + off;
-    for (int k = 0; k < ns; k += kSkInFlight) {
-        float4 v[kSkInFlight];
+    for (int k = 0; k < ns; k += NF) {
+        float4 v[NF];
 #pragma unroll
-        for (int u = 0; u < kSkInFlight; ++u)
+        for (int u = 0; u < NF; ++u)
             if (k + u < ns)
                 v[u] = __ldcs(reinterpret_cast<const float4*>(base + (int64_t)slots[k + u] * kTileElems));
 #pragma unroll
-        for (int u = 0; u < kSkInFlight; ++u) {
+        for (int u = 0; u < NF; ++u) {
             if (k + u < ns) {
                 acc.x += v[u].x;
                 acc.y += v[u].y;
@@ -1089,7 +1096,24 @@ cudaError_t launch_sk_fixup(const TcParams& p, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, sk_fixup_kernel, p);
+    // the batch width with the fewest (waves of blocks) x (load rounds): a
+    // tile meets at most ceil(sk_ctas / sk_tiles) + 1 shares
+    int num_sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        num_sms = p.sk_ctas;
+    const int64_t blocks = (int64_t)cfg.gridDim.x * cfg.gridDim.y;
+    const int slots = (p.sk_ctas + p.sk_tiles - 1) / p.sk_tiles + 1;
+    auto cost = [&](int nf, int per_sm) {
+        const int64_t conc = (int64_t)num_sms * per_sm;
+        return ((blocks + conc - 1) / conc) * (int64_t)((slots + nf - 1) / nf);
+    };
+    const int64_t c16 = cost(16, sk_fix_blocks_per_sm<16>());
+    const int64_t c8 = cost(8, sk_fix_blocks_per_sm<8>());
+    const int64_t c4 = cost(4, sk_fix_blocks_per_sm<4>());
+    if (c16 < c8 && c16 < c4) return cudaLaunchKernelEx(&cfg, sk_fixup_kernel<16>, p);
+    if (c8 < c4) return cudaLaunchKernelEx(&cfg, sk_fixup_kernel<8>, p);
+    return cudaLaunchKernelEx(&cfg, sk_fixup_kernel<4>, p);
 }
 
 cudaError_t launch_splitk_reduce(const float* ws_partial, int k_splits, int64_t M, int64_t N,
