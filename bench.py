@@ -489,8 +489,8 @@ def gram_flop(N, K, n_alpha=N_ALPHA):
 
 
 def run_full_pass(args, rank, world):
-    """BASELINE's fifth workload on a sample of decoder layers: one step is
-    one layer's whole pass.  The layers' inputs (3 GB of calibration tokens
+    """The full LLaMA-7B-shaped quantisation pass on a sample of decoder
+    layers: one step is one layer's whole pass.  The layers' inputs (3 GB of calibration tokens
     per layer) are generated on the host and uploaded before the timed region;
     they exceed L2 many times over, so no flush is needed."""
     import torch

@@ -3,12 +3,12 @@
  *
  * The method: "AWQ: Activation-aware Weight Quantization for On-Device LLM
  * Compression and Acceleration" (fdeinterviews.com/papers/awq).  Third
- * paragraph: multiplying a weight channel by s > 1 and dividing its input by
- * s leaves a layer's output unchanged while shrinking that channel's relative
- * rounding error; s is the channel's average activation magnitude raised to a
- * power alpha, and alpha comes from a quick grid search on a small
- * calibration set; every weight stays in low bits.  Seventh paragraph: only
- * activation statistics are collected.  First paragraph: decoding reads
+ * paragraph: scaling a weight channel up by s > 1 and its input down by the
+ * same factor keeps the layer's output while lowering that channel's
+ * relative rounding error; s is a power alpha of the channel's mean absolute
+ * activation, alpha is picked by trying a small grid of values on a few
+ * calibration samples, and all stored weights are low-bit.  Seventh
+ * paragraph: the method gathers activation statistics and fits nothing.  First paragraph: decoding reads
  * every weight once per step and is memory-bound, so 4-bit weights cut its
  * traffic about 4x.  The OpenAlex record of the same title (abstract):
  * on-the-fly dequantisation and kernel fusion in the inference kernels.
@@ -104,8 +104,8 @@ awq_status awq_candidate_scales(const double* mean_abs, int64_t K, const double*
 size_t awq_candidate_scales_workspace_size(int64_t K, int n_alpha);
 
 /* ---- step: alpha grid search ---------------------------------------------
- * For every alpha on the grid (third paragraph: "quick grid search on a
- * small calibration set", no backpropagation or reconstruction):
+ * For every alpha on the grid (third paragraph: alpha is searched on a few
+ * calibration samples, with no gradients and no refitting of weights):
  *   s = candidate scales (above); fake-quantise W diag(s) exactly as
  *   awq_pack_int4 does; E = Q(W diag(s)) diag(s)^-1 - W;
  *   mse(alpha) = ||Xcal E^T||_F^2 / (T N), the output MSE of
@@ -160,8 +160,8 @@ awq_status awq_search_scale_int3(const uint16_t* W, int64_t N, int64_t K, int64_
                                  awq_stream_t stream);
 
 /* ---- alpha search through the Gram matrix ---------------------------------
- * The pages' "quick grid search on a small calibration set" (third paragraph)
- * fixes the objective, not how it is evaluated.  ||Xcal E^T||_F^2 =
+ * The third paragraph picks alpha by a grid search on a few calibration
+ * samples: that fixes the objective, not how it is evaluated.  ||Xcal E^T||_F^2 =
  * tr(E G E^T) with G = Xcal^T Xcal, so once G is formed the per-alpha cost is
  * 2 N K^2 flops instead of 2 T N K: cheaper whenever T > K (a full
  * calibration set of 128 x 512 tokens).
@@ -222,7 +222,7 @@ awq_status awq_search_scale_noalloc(const uint16_t* W, int64_t N, int64_t K, int
                                     float* s_alpha_out, awq_stream_t stream);
 
 /* ---- step: INT4 packing --------------------------------------------------
- * Low-bit weights (third paragraph: "every weight stays in low bits"; last
+ * Low-bit weights (third paragraph: all stored weights are low-bit; last
  * paragraph: 4 bits).  Per row n and group g of 128 input channels:
  *   w'_k  = fp32(W[n,k] * s_k)                     (s_k = 1 when s is NULL)
  *   lo,hi = min, max of w' over the group

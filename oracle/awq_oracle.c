@@ -7,11 +7,12 @@
  *
  * Sources (the AWQ pages):
  *   - "AWQ: Activation-aware Weight Quantization for On-Device LLM Compression
- *     and Acceleration" (fdeinterviews.com/papers/awq), third paragraph: scale
- *     a weight channel by s > 1 and divide its input by s; s is each channel's
- *     average activation magnitude raised to a power alpha; alpha comes from a
- *     quick grid search on a small calibration set; every weight stays in low
- *     bits.  Seventh paragraph: only activation statistics are collected.
+ *     and Acceleration" (fdeinterviews.com/papers/awq), third paragraph: a
+ *     weight channel is scaled up by s > 1 and its input down by s; s is a
+ *     power alpha of the channel's mean absolute activation; alpha is picked
+ *     by trying a small grid on a few calibration samples; all stored
+ *     weights are low-bit.  Seventh paragraph: the method gathers activation
+ *     statistics and fits nothing.
  *     Fourth paragraph: the method was evaluated at 3 and 4 bits; last
  *     paragraph: 4 bits is the default, 3 bits possible with a noticeable
  *     gap.

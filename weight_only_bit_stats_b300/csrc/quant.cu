@@ -1,9 +1,9 @@
 // Candidate scales, INT4 packing and the search's final reduction.
 //
 // Method: "AWQ: Activation-aware Weight Quantization ..." (fdeinterviews.com
-// /papers/awq), third paragraph: s is each channel's average activation
-// magnitude raised to a power alpha, alpha from a grid search; every weight
-// stays in low bits.  Last paragraph: 4 bits.  Asymmetric levels 0..15 per
+// /papers/awq), third paragraph: s is a power alpha of the channel's mean
+// absolute activation, alpha is picked from a grid, and all stored weights
+// are low-bit.  Last paragraph: 4 bits.  Asymmetric levels 0..15 per
 // group of 128 with fp16 scale/zero are the library's stated format.
 #include "common.cuh"
 #include "kernels.cuh"
@@ -183,10 +183,10 @@ __device__ __forceinline__ bool fast_nibbles32(const float2* wp, float rcp, floa
 // the warp recomputes its levels with the exact quotient.
 //
 // BITS = 4: chunk 4j + c is packed word 4j + c of the row-group.  BITS = 3
-// ("3 and 4 bits", AWQ page, fourth paragraph): levels 0..7 in three bit
-// planes per 32-level block; block j is chunks 4j..4j+3, one per lane, so
-// the lanes' plane bytes are transposed across the four lanes (two shuffle
-// rounds with byte permutes) and lane c writes block c's three words.
+// (the AWQ page, fourth paragraph, evaluates 3 and 4 bits): levels 0..7 in
+// three bit planes per 32-level block; block j is chunks 4j..4j+3, one per
+// lane, so the lanes' plane bytes are transposed across the four lanes (two
+// shuffle rounds with byte permutes) and lane c writes block c's three words.
 template <int BITS>
 __global__ void __launch_bounds__(kPackThreads, kPackMinBlocks)
     pack_kernel(const uint16_t* __restrict__ W, int64_t N, int64_t K, int64_t ldw,

@@ -2,10 +2,10 @@
 //
 //  * W4A16 GEMM for M > 16 tokens: Y = X deq(Wq)^T.  Under large batches the
 //    matmul becomes compute-bound ("AWQ: Activation-aware Weight Quantization
-//    ...", fdeinterviews.com/papers/awq, "Weight-only quantization helps
-//    decoding most" paragraph); the packed tile is dequantised on the fly
-//    into shared memory and multiplied on the tensor cores (the OpenAlex
-//    record's abstract: on-the-fly dequantisation, kernel fusion).
+//    ...", fdeinterviews.com/papers/awq, ninth paragraph); the packed tile is
+//    dequantised on the fly into shared memory and multiplied on the tensor
+//    cores (the OpenAlex record's abstract: on-the-fly dequantisation, kernel
+//    fusion).
 //  * The alpha search (third paragraph: grid search over alpha on a small
 //    calibration set): per alpha, the producer fake-quantises W diag(s) with
 //    the exact rounding of the packer and writes the residual
