@@ -366,7 +366,7 @@ def test_pack_unpack_roundtrip(oracle_mod):
 
 def test_packed_bytes_quarter_of_fp16(oracle_mod):
     """4 bits per weight: a quarter of the fp16 bytes, plus 4 bytes of
-    scale/zero per group of 128 (pages: about a quarter of the memory)."""
+    scale/zero per group of 128 (the pages: roughly 4x less weight memory than fp16)."""
     W, _, _, _ = sg.layer_inputs(0, 3, 64, 1024, 0)
     qw, sc, ze = oracle_mod.pack_int4(W)
     assert qw.nbytes * 4 == W.nbytes
