@@ -146,6 +146,84 @@ def test_host_argument_checks(capi):
     assert capi.awq_last_error_string()
 
 
+def test_host_argument_checks_remaining_calls(capi):
+    """The entry points not exercised above refuse bad arguments on the host
+    too, with the documented codes (1 invalid argument, 2 shape, 3 alignment,
+    5 workspace), before any device call."""
+    buf = ctypes.create_string_buffer(4096 + 16)
+    base = (ctypes.addressof(buf) + 15) & ~15
+    alphas = (ctypes.c_double * 65)(*([0.0] * 65))
+    # mean of the statistics: token count, null pointers
+    assert capi.awq_act_mean(base, 0, 128, base, None) == 1
+    assert capi.awq_act_mean(None, 4, 128, base, None) == 1
+    assert capi.awq_act_mean(base, 4, 128, None, None) == 1
+    # candidate scales: K, n_alpha range, null pointers, workspace
+    ws = capi.awq_candidate_scales_workspace_size(128, 2)
+    assert ws > 0 and capi.awq_candidate_scales_workspace_size(0, 2) == 0
+    assert capi.awq_candidate_scales(base, 0, alphas, 2, base, base, ws, None) == 1
+    assert capi.awq_candidate_scales(base, 128, alphas, 0, base, base, ws, None) == 1
+    assert capi.awq_candidate_scales(base, 128, alphas, 65, base, base, ws, None) == 1
+    assert capi.awq_candidate_scales(None, 128, alphas, 2, base, base, ws, None) == 1
+    assert capi.awq_candidate_scales(base, 128, None, 2, base, base, ws, None) == 1
+    assert capi.awq_candidate_scales(base, 128, alphas, 2, None, base, ws, None) == 1
+    assert capi.awq_candidate_scales(base, 128, alphas, 2, base, None, ws, None) == 5
+    assert capi.awq_candidate_scales(base, 128, alphas, 2, base, base, ws - 1, None) == 5
+    assert capi.awq_candidate_scales(base, 128, alphas, 2, base, base + 8, ws, None) == 5
+    # 3-bit search: the same checks as the 4-bit search
+    args = dict(W=base, N=8, K=128, ldw=128, X=base, T=4, ldx=128, m=base, n_alpha=2,
+                group=128, s=base, best=base, ws=base, ws_bytes=4096)
+
+    def s3(**kw):
+        a = dict(args, **kw)
+        return capi.awq_search_scale_int3(a["W"], a["N"], a["K"], a["ldw"], a["X"], a["T"],
+                                          a["ldx"], a["m"], alphas, a["n_alpha"], a["group"],
+                                          a["s"], None, a["best"], None, a["ws"], a["ws_bytes"],
+                                          None)
+    assert s3(n_alpha=65) == 1 and s3(n_alpha=0) == 1 and s3(T=0) == 1
+    assert s3(W=None) == 1 and s3(best=None) == 1
+    assert s3(K=100, ldw=100, ldx=100) == 2 and s3(N=12) == 2 and s3(group=64) == 2
+    assert s3(ldx=132) == 2
+    assert s3(W=base + 2) == 3 and s3(s=base + 4) == 3
+    assert s3(ws=None, ws_bytes=0) == 5 and s3(ws_bytes=16) == 5
+    # 3-bit search through the Gram matrix
+
+    def g3(**kw):
+        a = dict(args, **kw)
+        return capi.awq_search_scale_gram_int3(a["W"], a["N"], a["K"], a["ldw"], a["X"], a["m"],
+                                               alphas, a["n_alpha"], a["group"], a["s"], None,
+                                               a["best"], None, a["ws"], a["ws_bytes"], None)
+    assert g3(n_alpha=65) == 1 and g3(X=None) == 1
+    assert g3(N=12) == 2 and g3(K=100, ldw=100) == 2
+    assert g3(X=base + 2) == 3
+    assert g3(ws=None, ws_bytes=0) == 5
+    # allocation-free search: sizes and n_alpha first, then the scratch size
+    # (a problem larger than the library's 16 MiB array)
+    assert capi.awq_search_scale_noalloc(base, 8, 128, 128, base, 4, 128, base, alphas, 65, 128,
+                                         base, None, base, None, None) == 1
+    assert capi.awq_search_scale_noalloc(base, 0, 128, 128, base, 4, 128, base, alphas, 2, 128,
+                                         base, None, base, None, None) == 1
+    assert capi.awq_search_workspace_size(8, 65536, 4, 64) > 16 << 20
+    assert capi.awq_search_scale_noalloc(base, 8, 65536, 65536, base, 4, 65536, base, alphas, 64,
+                                         128, base, None, base, None, None) == 5
+    # fused input scaling: null inv_s, then the matmul's own checks, and a
+    # misaligned inv_s
+    assert capi.w4a16_gemm_scaled(base, 1, 128, 128, None, base, base, base, 16, 128, base, 16,
+                                  None, 0, None) == 1
+    assert capi.w4a16_gemm_scaled(base, 1, 128, 128, base, base, base, base, 12, 128, base, 12,
+                                  None, 0, None) == 2
+    assert capi.w4a16_gemm_scaled(base, 1, 128, 128, base + 4, base, base, base, 16, 128, base,
+                                  16, None, 0, None) == 3
+    # its workspace: none at decode sizes; at least fp16(X / s) for M > 16
+    assert capi.w4a16_gemm_scaled_workspace_size(16, 4096, 4096) == 0
+    assert capi.w4a16_gemm_scaled_workspace_size(300, 4096, 4096) >= 300 * 4096 * 2
+    assert capi.w4a16_gemm_scaled_workspace_size(300, 4096, 100) == 0
+    assert capi.w4a16_gemm_scaled_workspace_size(300, 0, 4096) == 0
+    # the status word needs a device: without one the call reports that
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert capi.awq_sync_status(None) in (4, 6)
+
+
 def test_binding_refuses_cpu_tensors():
     torch = pytest.importorskip("torch")
     import weight_only_bit_stats_b300 as wb
