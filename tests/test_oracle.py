@@ -68,7 +68,8 @@ def test_fp16_rounding_ties_and_random(oracle_mod):
     for c in cases:
         x = np.concatenate([c, -c])
         got = oracle_mod.d2h_array(x)
-        ref = x.astype(np.float16).view(np.uint16)
+        with np.errstate(over="ignore"):        # values past 65520 round to inf
+            ref = x.astype(np.float16).view(np.uint16)
         assert np.array_equal(got, ref)
 
 
@@ -80,7 +81,8 @@ def test_fp16_fp32_inputs_dense_sample(oracle_mod):
     lows = np.arange(1 << 16, dtype=np.uint32)
     f32 = ((tops[:, None] << 16) | lows[None, :]).ravel().view(np.float32)
     got = oracle_mod.d2h_array(f32.astype(np.float64))
-    ref = f32.astype(np.float16).view(np.uint16)
+    with np.errstate(over="ignore"):            # the top binades round to inf
+        ref = f32.astype(np.float16).view(np.uint16)
     assert np.array_equal(got, ref)
 
 
